@@ -1,0 +1,223 @@
+/*
+ * libjtree — one decode step of causal parallel tree drafting (JetSpec) on a
+ * GB300 (sm_103a): per-depth top-W candidates, best-first tree expansion,
+ * the tree-causal mask, tree attention for the verification pass, and greedy
+ * acceptance.
+ *
+ * Sources (page title, site, section):
+ *   [PL] "JetSpec: Breaking the Scaling Ceiling of Speculative Decoding with
+ *        Parallel Tree Drafting", paperlayer.ai summary.
+ *   [SM] the same paper, Korean review on startedourmission.github.io.
+ *   [RB] the same paper, Chinese summary on paper.rainbus.top.
+ *   [PP] "JetSpec++: Foresight Parallel Drafting with Self Refinements",
+ *        paperlayer.ai summary.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every tensor pointer is a DEVICE pointer owned by the caller. The library
+ *   never allocates, frees or synchronises (except jt_read_device_error).
+ * - Every call is asynchronous on exec->stream and returns once the work is
+ *   enqueued. A NULL exec means the legacy default stream, no device error
+ *   word and no workspace.
+ * - Arguments are validated on the host before anything is launched; a bad
+ *   argument returns JT_ERR_INVALID_ARG or JT_ERR_UNSUPPORTED and launches
+ *   nothing. A failed launch returns JT_ERR_CUDA.
+ * - Values inside device buffers (parent ids, tokens, page ids, lengths) are
+ *   checked on the device. A bad value ORs a JT_DEVERR_* flag into
+ *   *exec->d_err (when non-NULL); the kernel then writes defined outputs
+ *   (zeros, acc_len 0) and never traps. jt_read_device_error fetches and
+ *   clears the word.
+ * - Calls that need scratch memory take it from exec->workspace (device,
+ *   caller-owned, 256-byte aligned, at least the size the matching
+ *   jt_*_workspace_bytes query returns). Two calls in flight at the same
+ *   time must not share a workspace.
+ * - Tree node ids are 0..n-1 in creation order with parent[v] < v; parent -1
+ *   means "child of the root". The root is the last prefix token, already in
+ *   the KV cache; it is not a tree node.
+ * - All pointers must be 16-byte aligned.
+ * - The library keeps no global state except a per-process cache of the
+ *   device's attributes; it is safe to call from several host threads.
+ */
+#ifndef JTREE_H_
+#define JTREE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* jt_stream_t;
+
+typedef enum {
+  JT_OK = 0,
+  JT_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, misaligned pointer */
+  JT_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. head_dim 96) */
+  JT_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  JT_ERR_DEVICE_DATA = 4,   /* jt_read_device_error found a device-side flag set */
+  JT_ERR_TIMEOUT = 5,       /* a bounded device-side wait expired (flag JT_DEVERR_TIMEOUT) */
+  JT_ERR_WORKSPACE = 6      /* exec->workspace missing or smaller than required */
+} jt_status;
+
+/* Bits of the device error word. */
+#define JT_DEVERR_PARENT   0x01  /* parent[v] outside [-1, v) */
+#define JT_DEVERR_TOKEN    0x02  /* a token id outside [0, vocab) */
+#define JT_DEVERR_NNODES   0x04  /* n_nodes outside [0, B] */
+#define JT_DEVERR_PAGE     0x08  /* a block-table page id outside the pool */
+#define JT_DEVERR_PREFIX   0x10  /* prefix_len outside [0, max_prefix] */
+#define JT_DEVERR_TIMEOUT  0x20  /* a bounded wait on an mbarrier ran out */
+
+typedef struct {
+  jt_stream_t stream;       /* stream every launch is enqueued on (NULL = default) */
+  int32_t* d_err;           /* optional device int32 error word; NULL = no reporting */
+  void* workspace;          /* optional caller-owned device scratch */
+  size_t workspace_bytes;   /* its size */
+} jt_exec;
+
+const char* jt_status_str(jt_status s);
+
+/* Synchronises exec->stream, copies *exec->d_err to *host_out and clears it.
+ * Returns JT_OK when the word was zero, JT_ERR_TIMEOUT when the timeout flag
+ * was set, JT_ERR_DEVICE_DATA for any other flag, JT_ERR_INVALID_ARG when
+ * exec or exec->d_err is NULL. */
+jt_status jt_read_device_error(const jt_exec* exec, int32_t* host_out);
+
+/* ------------------------------------------------------------------------
+ * jt_topw — top-W draft candidates per depth.
+ * [PL] App. E "Drafting": the proposer extracts the top-k tokens and their
+ * log-probabilities at each future position; [RB] "方法步骤详情": one draft
+ * pass yields logits for every depth and the top W candidates per depth.
+ *
+ *   logits : fp32 [batch][n_depth][vocab], row-major, read only
+ *   tok    : int32 [batch][n_depth][W]  token ids by logit, descending;
+ *            equal logits rank the lower token id first
+ *   logp   : fp32 [batch][n_depth][W]  log-softmax of those tokens over the
+ *            full vocabulary, x - m - log(sum_j exp(x_j - m))
+ * Limits: 1 <= W <= min(vocab, 32); vocab % 4 == 0; batch * n_depth >= 0.
+ * NaN logits are undefined; -inf is allowed as long as a row has one finite
+ * logit. Workspace: jt_topw_workspace_bytes (may be 0).
+ * ------------------------------------------------------------------------ */
+size_t jt_topw_workspace_bytes(int batch, int n_depth, int vocab, int W);
+jt_status jt_topw(const float* logits, int batch, int n_depth, int vocab, int W,
+                  int32_t* tok, float* logp, const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
+ * jt_tree_expand — budget-B best-first tree construction.
+ * [PL] App. B "Tree-Drafting Algorithm Details" (Algorithm 1) and §2 "Tree
+ * Construction and Verification"; [RB] "方法步骤详情"; branch score =
+ * cumulative draft log-probability, [SM] "How it works", s(π(v)) equation.
+ *
+ * Starting from the root (depth 0, score 0), repeatedly pop the expandable
+ * node with the highest score (ties: lower node id; the root first) and
+ * attach children r = 0..W-1 while fewer than B nodes exist. A child of a
+ * depth-d node takes token tok[b][d][r] (depth d+1's rank-r candidate) and
+ * score parent + logp[b][d][r] (one binary32 add). Children with depth < N
+ * are pushed back; stop when B nodes exist or nothing is expandable.
+ *
+ *   tok, logp : [batch][n_depth][W] (the output of jt_topw)
+ *   parent    : int32 [batch][B]  creation-order ids, -1 = child of root
+ *   token     : int32 [batch][B]
+ *   depth     : int32 [batch][B]  1..n_depth
+ *   score     : fp32  [batch][B]  cumulative log-prob
+ *   n_nodes   : int32 [batch]     nodes built (<= B); slots >= n_nodes hold
+ *               parent -1, token -1, depth 0, score 0
+ * Limits: 1 <= B <= 256, 1 <= n_depth <= 64, 1 <= W <= 32. No workspace.
+ * ------------------------------------------------------------------------ */
+jt_status jt_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W,
+                         int B, int32_t* parent, int32_t* token, int32_t* depth, float* score,
+                         int32_t* n_nodes, const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
+ * jt_tree_mask — tree-causal attention mask as ancestor bitmasks.
+ * [SM] "How it works", mask equation: M[v,u] = 0 iff u ∈ Anc(v) ∪ {v};
+ * [PL] App. E "Verification": the mask is applied without a dense
+ * per-request matrix.
+ *
+ *   parent  : int32 [batch][B], n_nodes : int32 [batch]
+ *   mask    : uint32 [batch][B][(B+31)/32]; bit (u & 31) of word (u >> 5)
+ *             of row v is set iff M[v,u] = 0. Rows v >= n_nodes are zero.
+ * Device check: parent[v] outside [-1, v) sets JT_DEVERR_PARENT and zeroes
+ * that sequence's rows. Limits: 1 <= B <= 256. No workspace.
+ * ------------------------------------------------------------------------ */
+jt_status jt_tree_mask(const int32_t* parent, const int32_t* n_nodes, int batch, int B,
+                       uint32_t* mask, const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
+ * jt_tree_attn — tree-causal GQA attention for the verification pass.
+ * [PL] §2 "Architecture" and App. E "Verification"; [SM] mask equation.
+ *
+ * For node v < n_nodes[b] and query head h (KV head h / (hq/hkv)):
+ *   o = softmax(scale * q K^T + mask) V over the keys
+ *       prefix[0 .. prefix_len[b])  ∪  { tree node u : mask[b][v] bit u }
+ * fp32 softmax and accumulation, bf16 output. Rows v >= n_nodes[b] are zero.
+ *
+ *   q            bf16 [batch][B][hq][D]
+ *   k_tree/v_tree bf16 [batch][B][hkv][D]   (the tree nodes' own K/V)
+ *   contiguous prefix (block_table == NULL):
+ *     k_cache/v_cache bf16 [batch][max_prefix][hkv][D]
+ *   paged prefix (block_table != NULL):
+ *     k_cache/v_cache bf16 [n_pages][page_size][hkv][D] pool,
+ *     block_table int32 [batch][max_pages]; token j of sequence b lives in
+ *     page block_table[b][j / page_size], slot j % page_size.
+ *   prefix_len   int32 [batch], n_nodes int32 [batch]
+ *   mask         uint32 [batch][B][(B+31)/32] (jt_tree_mask's output)
+ *   out          bf16 [batch][B][hq][D]
+ *   scale        0 means 1/sqrt(D)
+ * Limits: D in {64, 128}; hq % hkv == 0; hq/hkv <= 16; 1 <= B <= 256;
+ * page_size == 16 when paged. Workspace: jt_tree_attn_workspace_bytes.
+ * Device checks: prefix_len beyond max_prefix (or max_pages*page_size), a page
+ * id outside [0, n_pages) and n_nodes outside [0, B] set flags; the affected
+ * sequence's output is zero.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int batch, B, hq, hkv, head_dim;
+  float scale;
+  const void* q;
+  const void* k_tree;
+  const void* v_tree;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;   /* NULL = contiguous prefix */
+  int page_size, max_pages, n_pages;
+  int max_prefix;               /* contiguous: cache length; paged: 0 or a bound on prefix_len */
+  const int32_t* prefix_len;
+  const int32_t* n_nodes;
+  const uint32_t* mask;
+  void* out;
+} jt_attn_args;
+
+size_t jt_tree_attn_workspace_bytes(const jt_attn_args* args);
+jt_status jt_tree_attn(const jt_attn_args* args, const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
+ * jt_tree_accept — greedy (temperature 0) acceptance.
+ * [PL] §2 "Tree Construction and Verification": accept the longest prefix
+ * whose draft tokens meet the target's condition; [RB] "前置知识"; [PP] §3
+ * "Preliminaries": commit the accepted prefix plus one bonus token.
+ *
+ *   target  fp32 [batch][B+1][vocab]: row 0 is the target's prediction at the
+ *           root, row 1+v at node v. Argmax ties go to the lowest token id.
+ *   Walk: a = argmax(row 0); while a child c of the current node has
+ *   token[c] == a (the lowest id if several): accept c, a = argmax(row 1+c).
+ *   acc_len    int32 [batch]            accepted draft tokens (0..n_depth)
+ *   acc_tokens int32 [batch][n_depth]   their tokens, -1 beyond acc_len
+ *   acc_nodes  int32 [batch][n_depth]   their node ids, -1 beyond acc_len
+ *   bonus      int32 [batch]            the last argmax (committed too)
+ * Committed tokens this step = acc_len + 1.
+ * Limits: 1 <= B <= 256, 1 <= n_depth <= 64, vocab % 4 == 0.
+ * Workspace: jt_tree_accept_workspace_bytes. Device checks: bad parent, token
+ * or n_nodes set a flag and give acc_len 0, bonus -1 for that sequence.
+ * ------------------------------------------------------------------------ */
+size_t jt_tree_accept_workspace_bytes(int batch, int B, int vocab);
+jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, const int32_t* token,
+                         const int32_t* n_nodes, int batch, int B, int n_depth, int vocab,
+                         int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes,
+                         int32_t* bonus, const jt_exec* exec);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* JTREE_H_ */

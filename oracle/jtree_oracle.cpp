@@ -1,0 +1,358 @@
+// Oracle for one decode step of causal parallel tree drafting (JetSpec).
+//
+// TEST INFRASTRUCTURE ONLY. Nothing in the product path may link, import or
+// call this file: only tests/, __graft_entry__.smoke() and bench.py's
+// cpu_baseline / --impl reference legs use it. It shares no code, header,
+// table or helper with the CUDA library; the two meet only at the seeded
+// input bytes.
+//
+// Plain, slow, single-threaded C++17 written from the definitions on the
+// pages (compiled with -O2 -ffp-contract=off, no fast-math):
+//   orc_tree_mask    - the tree-causal mask M[v,u] (explicit ancestor walk)
+//   orc_tree_attn    - attention with an explicit dense mask, fp64 softmax
+//   orc_topw         - full stable sort of the vocabulary + fp64 log-softmax
+//   orc_tree_expand  - best-first expansion on a std::priority_queue
+//   orc_tree_accept  - sequential argmax + walk down the tree
+//
+// Sources (page title, site, section):
+//   [PL]  "JetSpec: Breaking the Scaling Ceiling of Speculative Decoding with
+//         Parallel Tree Drafting", paperlayer.ai summary.
+//   [SM]  the same paper, Korean review on startedourmission.github.io.
+//   [RB]  the same paper, Chinese summary on paper.rainbus.top.
+//   [PP]  "JetSpec++: Foresight Parallel Drafting with Self Refinements",
+//         paperlayer.ai summary.
+//
+// Every function returns 0 on success and a negative code on bad input
+// (it never aborts), so tests can drive it with hand-made bad trees.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <numeric>
+#include <queue>
+#include <vector>
+
+namespace {
+
+constexpr int kBadArg = -1;
+constexpr int kBadTree = -2;
+constexpr int kBadToken = -3;
+
+double widen_bf16(uint16_t bits) {
+  // A bf16 value is the top half of an IEEE binary32; widening is exact.
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+// Tree-causal mask. [SM] "How it works", mask equation:
+//   M[v,u] = 0 if u in Anc(v) ∪ {v}, else -inf.
+// [PL] §2 "Architecture": every node sees the prefix and its own ancestors,
+// never descendants or unrelated siblings.
+// Node ids are 0..n-1 in creation order; parent[v] = -1 means "child of the
+// root" (the root is the last prefix token and is not a tree node).
+// Output: for each node v a row of ceil(B/32) uint32 words, bit (u & 31) of
+// word (u >> 5) set iff M[v,u] = 0. Rows v >= n are zero.
+// Returns kBadTree if some parent[v] is outside [-1, v).
+// ---------------------------------------------------------------------------
+int orc_tree_mask(const int32_t* parent, const int32_t* n_nodes, int batch, int B,
+                  uint32_t* mask) {
+  if (batch < 0 || B < 0) return kBadArg;
+  const int words = (B + 31) / 32;
+  std::fill(mask, mask + static_cast<size_t>(batch) * B * words, 0u);
+  for (int b = 0; b < batch; ++b) {
+    const int n = n_nodes[b];
+    if (n < 0 || n > B) return kBadTree;
+    const int32_t* par = parent + static_cast<size_t>(b) * B;
+    for (int v = 0; v < n; ++v)
+      if (par[v] < -1 || par[v] >= v) return kBadTree;
+    // Dense boolean matrix first, exactly as the definition reads.
+    std::vector<char> visible(static_cast<size_t>(n) * n, 0);
+    for (int v = 0; v < n; ++v) {
+      visible[static_cast<size_t>(v) * n + v] = 1;  // u = v
+      for (int u = par[v]; u != -1; u = par[u])      // u in Anc(v)
+        visible[static_cast<size_t>(v) * n + u] = 1;
+    }
+    for (int v = 0; v < n; ++v)
+      for (int u = 0; u < n; ++u)
+        if (visible[static_cast<size_t>(v) * n + u])
+          mask[(static_cast<size_t>(b) * B + v) * words + (u >> 5)] |= 1u << (u & 31);
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Tree-causal GQA attention for the verification pass.
+// [PL] App. E "Verification": the target verifies every node in one forward
+// pass using the tree attention mask; [PL] §2: each node attends to the
+// prefix plus its ancestors and itself.
+//
+// For node v of sequence b and query head h (KV head h / (hq / hkv)):
+//   keys  = prefix tokens 0..L_b-1  ∪  tree nodes u < n_b
+//   s_j   = scale * <q, k_j>, plus the mask term (0 or -inf) for tree keys
+//   out   = sum_j softmax(s)_j v_j
+// Everything after widening the bf16 inputs is done in double.
+//
+// Layouts (element = bf16 bit pattern, uint16):
+//   q, out rows : [batch][B][hq][D]   (out is double)
+//   k/v_tree    : [batch][B][hkv][D]
+//   contiguous prefix (block_table == NULL): [batch][max_prefix][hkv][D]
+//   paged prefix: pool [pages][page_size][hkv][D], token j of sequence b in
+//                 page block_table[b * max_pages + j / page_size], slot
+//                 j % page_size.
+// rows / n_rows: optional list of (b, v, h) triples to compute; out then has
+// n_rows rows of D doubles. rows == NULL computes all batch*B*hq rows.
+// Rows with v >= n_b are zero.
+// ---------------------------------------------------------------------------
+int orc_tree_attn(int batch, int B, int hq, int hkv, int D, double scale,
+                  const uint16_t* q, const uint16_t* k_tree, const uint16_t* v_tree,
+                  const uint16_t* k_cache, const uint16_t* v_cache,
+                  const int32_t* block_table, int page_size, int max_pages,
+                  int max_prefix, int n_pool_pages,
+                  const int32_t* prefix_len, const int32_t* n_nodes,
+                  const uint32_t* mask, const int32_t* rows, int n_rows, double* out) {
+  if (batch < 0 || B < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || D <= 0) return kBadArg;
+  const int g = hq / hkv;
+  const int words = (B + 31) / 32;
+  if (scale == 0.0) scale = 1.0 / std::sqrt(static_cast<double>(D));
+  const long total = rows ? n_rows : static_cast<long>(batch) * B * hq;
+
+  std::vector<double> s, qv(D), acc(D);
+  for (long r = 0; r < total; ++r) {
+    int b, v, h;
+    if (rows) {
+      b = rows[3 * r]; v = rows[3 * r + 1]; h = rows[3 * r + 2];
+      if (b < 0 || b >= batch || v < 0 || v >= B || h < 0 || h >= hq) return kBadArg;
+    } else {
+      b = static_cast<int>(r / (static_cast<long>(B) * hq));
+      v = static_cast<int>((r / hq) % B);
+      h = static_cast<int>(r % hq);
+    }
+    double* o = out + r * D;
+    std::fill(o, o + D, 0.0);
+    const int n = n_nodes[b];
+    const int L = prefix_len[b];
+    if (n < 0 || n > B) return kBadTree;
+    if (v >= n) continue;  // unused budget slot: defined as zero
+    if (L < 0 || (!block_table && L > max_prefix) ||
+        (block_table && L > max_pages * page_size)) return kBadArg;
+    const int kh = h / g;
+
+    const uint16_t* qrow = q + ((static_cast<size_t>(b) * B + v) * hq + h) * D;
+    for (int d = 0; d < D; ++d) qv[d] = widen_bf16(qrow[d]);
+
+    auto prefix_row = [&](const uint16_t* base, int j) -> const uint16_t* {
+      size_t tok;
+      if (block_table) {
+        const int page = block_table[static_cast<size_t>(b) * max_pages + j / page_size];
+        if (page < 0 || page >= n_pool_pages) return nullptr;
+        tok = static_cast<size_t>(page) * page_size + j % page_size;
+      } else {
+        tok = static_cast<size_t>(b) * max_prefix + j;
+      }
+      return base + (tok * hkv + kh) * D;
+    };
+    auto tree_row = [&](const uint16_t* base, int u) -> const uint16_t* {
+      return base + ((static_cast<size_t>(b) * B + u) * hkv + kh) * D;
+    };
+
+    // Scores over all L + n keys; the dense mask term is explicit.
+    const double neg_inf = -std::numeric_limits<double>::infinity();
+    s.assign(static_cast<size_t>(L) + n, 0.0);
+    for (int j = 0; j < L; ++j) {
+      const uint16_t* kr = prefix_row(k_cache, j);
+      if (!kr) return kBadArg;
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qv[d] * widen_bf16(kr[d]);
+      s[j] = scale * dot;
+    }
+    const uint32_t* mrow = mask + (static_cast<size_t>(b) * B + v) * words;
+    for (int u = 0; u < n; ++u) {
+      const bool visible = (mrow[u >> 5] >> (u & 31)) & 1u;
+      double dot = 0.0;
+      const uint16_t* kr = tree_row(k_tree, u);
+      for (int d = 0; d < D; ++d) dot += qv[d] * widen_bf16(kr[d]);
+      s[L + u] = scale * dot + (visible ? 0.0 : neg_inf);
+    }
+    // Max-subtracted softmax; a row with no visible key stays zero.
+    double m = neg_inf;
+    for (double x : s) m = std::max(m, x);
+    if (m == neg_inf) continue;
+    double denom = 0.0;
+    std::fill(acc.begin(), acc.end(), 0.0);
+    for (size_t j = 0; j < s.size(); ++j) {
+      if (s[j] == neg_inf) continue;
+      const double p = std::exp(s[j] - m);
+      denom += p;
+      const uint16_t* vr = (static_cast<int>(j) < L) ? prefix_row(v_cache, static_cast<int>(j))
+                                                       : tree_row(v_tree, static_cast<int>(j) - L);
+      for (int d = 0; d < D; ++d) acc[d] += p * widen_bf16(vr[d]);
+    }
+    for (int d = 0; d < D; ++d) o[d] = acc[d] / denom;
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Per-depth top-W candidates. [PL] App. E "Drafting": the proposer takes the
+// top-k tokens and their log-probabilities at each future position;
+// [RB] "方法步骤详情" (inference): one draft pass gives logits for every
+// depth, and the top W candidates are extracted per depth.
+//
+// For each row (b, d) of V fp32 logits:
+//   order  : full stable sort of token ids by logit, descending (ties keep
+//            the lower id first), take the first W;
+//   logp_i : x_i - m - log(sum_j exp(x_j - m)), m = max_j x_j, in double,
+//            rounded once to float.
+// ---------------------------------------------------------------------------
+int orc_topw(const float* logits, int batch, int n_depth, int vocab, int W,
+             int32_t* tok, float* logp) {
+  if (batch < 0 || n_depth < 0 || vocab <= 0 || W <= 0 || W > vocab) return kBadArg;
+  std::vector<int32_t> idx(vocab);
+  for (long row = 0; row < static_cast<long>(batch) * n_depth; ++row) {
+    const float* x = logits + row * static_cast<long>(vocab);
+    double m = -std::numeric_limits<double>::infinity();
+    for (int j = 0; j < vocab; ++j) m = std::max(m, static_cast<double>(x[j]));
+    double Z = 0.0;
+    for (int j = 0; j < vocab; ++j) Z += std::exp(static_cast<double>(x[j]) - m);
+    const double logZ = std::log(Z);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [x](int32_t a, int32_t c) { return x[a] > x[c]; });
+    for (int r = 0; r < W; ++r) {
+      tok[row * W + r] = idx[r];
+      logp[row * W + r] = static_cast<float>(static_cast<double>(x[idx[r]]) - m - logZ);
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Best-first tree expansion. [PL] App. B "Tree-Drafting Algorithm Details"
+// (Algorithm 1) and [PL] §2 "Tree Construction and Verification"; [RB]
+// "方法步骤详情": repeatedly pop the highest-scoring expandable node, attach
+// up to W children, re-insert the children with updated scores, until the
+// budget is full or no expandable node remains. Score = cumulative draft
+// log-probability along the path, [SM] "How it works", s(π(v)) equation.
+//
+// Readings where the pages are silent:
+//   * the budget B counts draft nodes, not the root;
+//   * a child of a depth-d node takes its token and log-prob from depth
+//     d+1's top-W list (rank order), shared by every depth-d node;
+//   * children are attached in rank order while fewer than B nodes exist;
+//     depth-N children are created but never pushed (not expandable);
+//   * score(child) = score(parent) + logp in binary32 (the precision the
+//     kernel ranks in), heap order = (score desc, node id asc), the root
+//     (id -1, score 0) is popped first.
+// tok/logp: [batch][n_depth][W] as produced by orc_topw.
+// Outputs per sequence: parent/token/depth/score [B] (slots >= n set to
+// -1/-1/0/0), n_nodes.
+// ---------------------------------------------------------------------------
+int orc_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W, int B,
+                    int32_t* parent, int32_t* token, int32_t* depth, float* score,
+                    int32_t* n_nodes) {
+  if (batch < 0 || n_depth <= 0 || W <= 0 || B < 0) return kBadArg;
+  struct Entry { float score; int32_t id; int32_t depth; };
+  struct Lower {  // "a ranks below c" for std::priority_queue (max-heap)
+    bool operator()(const Entry& a, const Entry& c) const {
+      if (a.score != c.score) return a.score < c.score;
+      return a.id > c.id;
+    }
+  };
+  for (int b = 0; b < batch; ++b) {
+    int32_t* par = parent + static_cast<size_t>(b) * B;
+    int32_t* tk = token + static_cast<size_t>(b) * B;
+    int32_t* dp = depth + static_cast<size_t>(b) * B;
+    float* sc = score + static_cast<size_t>(b) * B;
+    for (int v = 0; v < B; ++v) { par[v] = -1; tk[v] = -1; dp[v] = 0; sc[v] = 0.0f; }
+    const int32_t* tok_b = tok + static_cast<size_t>(b) * n_depth * W;
+    const float* logp_b = logp + static_cast<size_t>(b) * n_depth * W;
+
+    std::priority_queue<Entry, std::vector<Entry>, Lower> heap;
+    heap.push(Entry{0.0f, -1, 0});
+    int count = 0;
+    while (count < B && !heap.empty()) {
+      const Entry u = heap.top();
+      heap.pop();
+      const int d = u.depth + 1;  // depth of the children, 1..N
+      for (int r = 0; r < W && count < B; ++r) {
+        const int v = count++;
+        par[v] = u.id;
+        tk[v] = tok_b[(d - 1) * W + r];
+        dp[v] = d;
+        sc[v] = u.score + logp_b[(d - 1) * W + r];  // one binary32 add
+        if (d < n_depth) heap.push(Entry{sc[v], v, d});
+      }
+    }
+    n_nodes[b] = count;
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Greedy tree acceptance. [PL] §2 "Tree Construction and Verification":
+// verification accepts the longest prefix whose draft tokens satisfy the
+// target's acceptance condition; [RB] "前置知识": the target keeps the longest
+// prefix consistent with its own predictions; [PP] §3 "Preliminaries": the
+// accepted prefix is committed together with one bonus token.
+// At temperature 0 the condition is "token == target argmax at the parent".
+//
+// target: [batch][B+1][V] fp32, row 0 = the root's prediction, row 1+v =
+// node v's prediction. Argmax ties go to the lowest token id.
+// Walk: a = argmax(row 0); while some child c of the current node has
+// token[c] == a (the lowest such id if several): accept c, a = argmax(row
+// 1+c). bonus = the last a. acc_tokens/acc_nodes: [batch][n_depth], unused
+// entries -1. Returns kBadTree for a parent outside [-1, v).
+// ---------------------------------------------------------------------------
+int orc_tree_accept(const float* target, const int32_t* parent, const int32_t* token,
+                    const int32_t* n_nodes, int batch, int B, int n_depth, int vocab,
+                    int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus) {
+  if (batch < 0 || B < 0 || n_depth <= 0 || vocab <= 0) return kBadArg;
+  auto argmax = [vocab](const float* row) {
+    int best = 0;
+    for (int j = 1; j < vocab; ++j)
+      if (row[j] > row[best]) best = j;
+    return best;
+  };
+  for (int b = 0; b < batch; ++b) {
+    const int n = n_nodes[b];
+    if (n < 0 || n > B) return kBadTree;
+    const int32_t* par = parent + static_cast<size_t>(b) * B;
+    const int32_t* tk = token + static_cast<size_t>(b) * B;
+    for (int v = 0; v < n; ++v) {
+      if (par[v] < -1 || par[v] >= v) return kBadTree;
+      if (tk[v] < 0 || tk[v] >= vocab) return kBadToken;
+    }
+    const float* rows = target + static_cast<size_t>(b) * (B + 1) * vocab;
+    int32_t* at = acc_tokens + static_cast<size_t>(b) * n_depth;
+    int32_t* an = acc_nodes + static_cast<size_t>(b) * n_depth;
+    for (int i = 0; i < n_depth; ++i) { at[i] = -1; an[i] = -1; }
+
+    int cur = -1;
+    int a = argmax(rows);
+    int len = 0;
+    while (true) {
+      int next = -1;
+      for (int c = 0; c < n; ++c)
+        if (par[c] == cur && tk[c] == a) { next = c; break; }
+      if (next < 0 || len >= n_depth) break;
+      at[len] = a;
+      an[len] = next;
+      ++len;
+      cur = next;
+      a = argmax(rows + static_cast<size_t>(1 + next) * vocab);
+    }
+    acc_len[b] = len;
+    bonus[b] = a;
+  }
+  return 0;
+}
+
+}  // extern "C"
