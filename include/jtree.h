@@ -44,6 +44,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define JT_API __attribute__((visibility("default")))
+#else
+#define JT_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -76,13 +82,13 @@ typedef struct {
   size_t workspace_bytes;   /* its size */
 } jt_exec;
 
-const char* jt_status_str(jt_status s);
+JT_API const char* jt_status_str(jt_status s);
 
 /* Synchronises exec->stream, copies *exec->d_err to *host_out and clears it.
  * Returns JT_OK when the word was zero, JT_ERR_TIMEOUT when the timeout flag
  * was set, JT_ERR_DEVICE_DATA for any other flag, JT_ERR_INVALID_ARG when
  * exec or exec->d_err is NULL. */
-jt_status jt_read_device_error(const jt_exec* exec, int32_t* host_out);
+JT_API jt_status jt_read_device_error(const jt_exec* exec, int32_t* host_out);
 
 /* ------------------------------------------------------------------------
  * jt_topw — top-W draft candidates per depth.
@@ -99,8 +105,8 @@ jt_status jt_read_device_error(const jt_exec* exec, int32_t* host_out);
  * NaN logits are undefined; -inf is allowed as long as a row has one finite
  * logit. Workspace: jt_topw_workspace_bytes (may be 0).
  * ------------------------------------------------------------------------ */
-size_t jt_topw_workspace_bytes(int batch, int n_depth, int vocab, int W);
-jt_status jt_topw(const float* logits, int batch, int n_depth, int vocab, int W,
+JT_API size_t jt_topw_workspace_bytes(int batch, int n_depth, int vocab, int W);
+JT_API jt_status jt_topw(const float* logits, int batch, int n_depth, int vocab, int W,
                   int32_t* tok, float* logp, const jt_exec* exec);
 
 /* ------------------------------------------------------------------------
@@ -125,7 +131,7 @@ jt_status jt_topw(const float* logits, int batch, int n_depth, int vocab, int W,
  *               parent -1, token -1, depth 0, score 0
  * Limits: 1 <= B <= 256, 1 <= n_depth <= 64, 1 <= W <= 32. No workspace.
  * ------------------------------------------------------------------------ */
-jt_status jt_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W,
+JT_API jt_status jt_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W,
                          int B, int32_t* parent, int32_t* token, int32_t* depth, float* score,
                          int32_t* n_nodes, const jt_exec* exec);
 
@@ -141,7 +147,7 @@ jt_status jt_tree_expand(const int32_t* tok, const float* logp, int batch, int n
  * Device check: parent[v] outside [-1, v) sets JT_DEVERR_PARENT and zeroes
  * that sequence's rows. Limits: 1 <= B <= 256. No workspace.
  * ------------------------------------------------------------------------ */
-jt_status jt_tree_mask(const int32_t* parent, const int32_t* n_nodes, int batch, int B,
+JT_API jt_status jt_tree_mask(const int32_t* parent, const int32_t* n_nodes, int batch, int B,
                        uint32_t* mask, const jt_exec* exec);
 
 /* ------------------------------------------------------------------------
@@ -188,8 +194,8 @@ typedef struct {
   void* out;
 } jt_attn_args;
 
-size_t jt_tree_attn_workspace_bytes(const jt_attn_args* args);
-jt_status jt_tree_attn(const jt_attn_args* args, const jt_exec* exec);
+JT_API size_t jt_tree_attn_workspace_bytes(const jt_attn_args* args);
+JT_API jt_status jt_tree_attn(const jt_attn_args* args, const jt_exec* exec);
 
 /* ------------------------------------------------------------------------
  * jt_tree_accept — greedy (temperature 0) acceptance.
@@ -210,8 +216,8 @@ jt_status jt_tree_attn(const jt_attn_args* args, const jt_exec* exec);
  * Workspace: jt_tree_accept_workspace_bytes. Device checks: bad parent, token
  * or n_nodes set a flag and give acc_len 0, bonus -1 for that sequence.
  * ------------------------------------------------------------------------ */
-size_t jt_tree_accept_workspace_bytes(int batch, int B, int vocab);
-jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, const int32_t* token,
+JT_API size_t jt_tree_accept_workspace_bytes(int batch, int B, int vocab);
+JT_API jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, const int32_t* token,
                          const int32_t* n_nodes, int batch, int B, int n_depth, int vocab,
                          int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes,
                          int32_t* bonus, const jt_exec* exec);

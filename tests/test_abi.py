@@ -1,0 +1,66 @@
+"""The C-ABI library loads and exports every symbol include/jtree.h declares.
+
+Runs without a GPU: only symbol lookup, the status strings, the workspace
+size queries and argument checks that fail before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tree_causal_verification_gb300 import build, jtree
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "jtree.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"JT_API\s+[\w\s\*]+?\b(jt_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return jtree.load()
+
+
+def test_header_declares_the_five_calls():
+    syms = declared_symbols()
+    for name in ("jt_topw", "jt_tree_expand", "jt_tree_mask", "jt_tree_attn", "jt_tree_accept"):
+        assert name in syms
+    assert set(syms) <= set(jtree.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in jtree.STATUS_NAMES.items():
+        assert lib.jt_status_str(code).decode().startswith(name)
+
+
+def test_host_validation_needs_no_gpu(lib):
+    ex = jtree.jt_exec()
+    # W = 0, B = 300, bad head_dim: rejected before any CUDA call.
+    assert lib.jt_topw(None, 1, 1, 8, 0, None, None, ctypes.byref(ex)) == 1
+    assert lib.jt_tree_expand(None, None, 1, 4, 2, 300, None, None, None, None, None,
+                              ctypes.byref(ex)) == 1
+    assert lib.jt_tree_mask(None, None, 1, 0, None, ctypes.byref(ex)) == 1
+    args = jtree.jt_attn_args(1, 16, 32, 8, 96, 0.0)
+    assert lib.jt_tree_attn(ctypes.byref(args), ctypes.byref(ex)) == 2
+    args = jtree.jt_attn_args(1, 16, 30, 8, 128, 0.0)  # hq % hkv != 0
+    assert lib.jt_tree_attn(ctypes.byref(args), ctypes.byref(ex)) == 1
+    assert lib.jt_tree_accept(None, None, None, None, 1, 16, 0, 1024, None, None, None, None,
+                              ctypes.byref(ex)) == 1
+    assert lib.jt_read_device_error(None, None) == 1
+
+
+def test_workspace_queries(lib):
+    assert lib.jt_tree_accept_workspace_bytes(64, 128, 151936) >= 64 * 129 * 4
+    assert lib.jt_tree_accept_workspace_bytes(64, 128, 151936) % 256 == 0
+    assert lib.jt_topw_workspace_bytes(1, 16, 151936, 4) == 0

@@ -1,0 +1,136 @@
+// jt_tree_expand: budget-B best-first tree construction.
+//
+// Algorithm (JetSpec summary on paperlayer.ai, App. B "Tree-Drafting
+// Algorithm Details", Algorithm 1, and §2 "Tree Construction and
+// Verification"; Chinese summary on paper.rainbus.top, "方法步骤详情"): pop the
+// expandable node with the highest cumulative log-prob (JetSpec review on
+// startedourmission.github.io, "How it works", s(π(v)) equation), attach up
+// to W children, push them back, until B nodes exist or nothing is left.
+//
+// GPU design: the expansion is inherently serial, so one warp owns one
+// sequence and makes every step of a pop warp-parallel instead of using a
+// heap. The frontier (created, unpopped nodes with depth < N) lives in
+// registers: node v occupies lane v & 31, slot v >> 5 (B <= 256 -> 8 slots).
+// A pop is two warp reductions: __reduce_max_sync over an order-preserving
+// uint32 key of the score, then __reduce_min_sync over the ids holding that
+// key (ties -> lower id, as the heap order requires). The W children of a
+// pop are created by W lanes at once; each is handed to its owner lane by a
+// shuffle. Scores are binary32 sums (__fadd_rn), the same adds as the
+// definition.
+#include <climits>
+
+#include "jt_internal.cuh"
+
+namespace jt {
+namespace {
+
+constexpr int kWarpsPerBlock = 4;
+
+template <int SLOTS>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ logp, int batch,
+                   int N, int W, int B, int32_t* __restrict__ parent_o,
+                   int32_t* __restrict__ token_o, int32_t* __restrict__ depth_o,
+                   float* __restrict__ score_o, int32_t* __restrict__ n_nodes_o) {
+  __shared__ uint8_t depth_s[kWarpsPerBlock][kMaxB];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kWarpsPerBlock + warp;
+  if (b >= batch) return;  // whole warp leaves together
+  constexpr unsigned kFull = 0xFFFFFFFFu;
+
+  const int32_t* tk = tok + (size_t)b * N * W;
+  const float* lp = logp + (size_t)b * N * W;
+  int32_t* par = parent_o + (size_t)b * B;
+  int32_t* tko = token_o + (size_t)b * B;
+  int32_t* dpo = depth_o + (size_t)b * B;
+  float* sco = score_o + (size_t)b * B;
+  uint8_t* dep = depth_s[warp];
+
+  float fs[SLOTS];
+#pragma unroll
+  for (int k = 0; k < SLOTS; ++k) fs[k] = 0.0f;
+  uint32_t alive = 0;  // bit k: slot k holds a frontier node
+
+  int count = 0;
+  int cur = -1;          // the node being expanded; the root first
+  float cur_s = 0.0f;
+  int cur_d = 0;
+  while (true) {
+    const int d = cur_d + 1;               // depth of the children
+    const int nc = min(W, B - count);
+    float csc = 0.0f;
+    if (lane < nc) {                       // lane r creates child r
+      const int v = count + lane;
+      const int t = __ldg(tk + (d - 1) * W + lane);
+      csc = __fadd_rn(cur_s, __ldg(lp + (d - 1) * W + lane));
+      par[v] = cur;
+      tko[v] = t;
+      dpo[v] = d;
+      sco[v] = csc;
+      dep[v] = (uint8_t)d;
+    }
+    // Owner lane of child v = count + r is lane v & 31, i.e. r = (lane - count) & 31.
+    const int r = (lane - count) & 31;
+    const float sv = __shfl_sync(kFull, csc, r);
+    if (d < N && r < nc) {
+      const int slot = (count + r) >> 5;
+#pragma unroll
+      for (int k = 0; k < SLOTS; ++k)
+        if (k == slot) fs[k] = sv;
+      alive |= 1u << slot;
+    }
+    count += nc;
+    __syncwarp();
+    if (count >= B) break;
+
+    // Pop: best (key desc, id asc) over the frontier.
+    uint32_t key = 0;   // 0 = empty (every float maps above 0)
+    int slot_best = 0;
+    float val_best = 0.0f;
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+      if ((alive >> k) & 1u) {
+        const uint32_t kk = order_key(fs[k]);
+        if (kk > key) { key = kk; slot_best = k; val_best = fs[k]; }
+      }
+    }
+    const uint32_t top = __reduce_max_sync(kFull, key);
+    if (top == 0) break;  // nothing expandable
+    const uint32_t my_id = (key == top) ? (uint32_t)((slot_best << 5) | lane) : 0xFFFFFFFFu;
+    const uint32_t id = __reduce_min_sync(kFull, my_id);
+    const int owner = (int)(id & 31u);
+    cur_s = __shfl_sync(kFull, val_best, owner);
+    if (lane == owner) alive &= ~(1u << (id >> 5));
+    cur = (int)id;
+    cur_d = dep[cur];
+  }
+  for (int v = count + lane; v < B; v += 32) {
+    par[v] = -1;
+    tko[v] = -1;
+    dpo[v] = 0;
+    sco[v] = 0.0f;
+  }
+  if (lane == 0) n_nodes_o[b] = count;
+}
+
+}  // namespace
+
+cudaError_t launch_tree_expand(const Ctx& c, const int32_t* tok, const float* logp, int batch,
+                               int n_depth, int W, int B, int32_t* parent, int32_t* token,
+                               int32_t* depth, float* score, int32_t* n_nodes) {
+  if (batch == 0) return cudaSuccess;
+  const int slots = (B + 31) / 32;
+  dim3 grid((batch + kWarpsPerBlock - 1) / kWarpsPerBlock), block(kWarpsPerBlock * 32);
+#define JT_EXPAND(S)                                                                       \
+  tree_expand_kernel<S><<<grid, block, 0, c.stream>>>(tok, logp, batch, n_depth, W, B,     \
+                                                       parent, token, depth, score, n_nodes)
+  if (slots <= 1) JT_EXPAND(1);
+  else if (slots <= 2) JT_EXPAND(2);
+  else if (slots <= 4) JT_EXPAND(4);
+  else JT_EXPAND(8);
+#undef JT_EXPAND
+  return cudaGetLastError();
+}
+
+}  // namespace jt

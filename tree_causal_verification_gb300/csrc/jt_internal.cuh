@@ -1,0 +1,74 @@
+// Internal declarations shared by libjtree's translation units.
+// Not part of the public ABI (that is include/jtree.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/jtree.h"
+
+namespace jt {
+
+constexpr int kMaxB = 256;        // tree budget limit (8 mask words per row)
+constexpr int kMaxWords = kMaxB / 32;
+constexpr int kMaxDepth = 64;
+constexpr int kMaxW = 32;
+constexpr int kPageSize = 16;
+constexpr int kNumSMs = 152;      // GB300; the launchers query the real count
+
+// ---------------------------------------------------------------------------
+// Device error word.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void raise_flag(int32_t* d_err, int32_t bit) {
+  if (d_err) atomicOr(d_err, bit);
+}
+
+// Float -> uint32 key whose unsigned order is the float order, with -0 == +0
+// (the caller folds -0 to +0 first). NaN is outside the contract.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// (value, index) ranking used by every top-W / argmax in the library:
+// a ranks before b iff a.v > b.v, or a.v == b.v and a.i < b.i.
+__device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// ---------------------------------------------------------------------------
+// Launch plumbing shared by jt_api.cu and the kernel files.
+// ---------------------------------------------------------------------------
+struct Ctx {
+  cudaStream_t stream;
+  int32_t* d_err;
+  void* workspace;
+  size_t workspace_bytes;
+  int num_sms;
+  int device;
+};
+
+// Device attributes are cached per device (the only process-wide state).
+int device_sm_count(int device);
+
+// Launchers (defined next to their kernels). They assume validated args and
+// return the cudaError_t of the launch.
+cudaError_t launch_tree_mask(const Ctx&, const int32_t* parent, const int32_t* n_nodes, int batch,
+                             int B, uint32_t* mask);
+cudaError_t launch_tree_expand(const Ctx&, const int32_t* tok, const float* logp, int batch,
+                               int n_depth, int W, int B, int32_t* parent, int32_t* token,
+                               int32_t* depth, float* score, int32_t* n_nodes);
+cudaError_t launch_topw(const Ctx&, const float* logits, int rows, int vocab, int W, int32_t* tok,
+                        float* logp);
+size_t accept_workspace_bytes(int batch, int B, int vocab);
+cudaError_t launch_tree_accept(const Ctx&, const float* target, const int32_t* parent,
+                               const int32_t* token, const int32_t* n_nodes, int batch, int B,
+                               int n_depth, int vocab, int32_t* acc_len, int32_t* acc_tokens,
+                               int32_t* acc_nodes, int32_t* bonus);
+size_t attn_workspace_bytes(const jt_attn_args& a, int num_sms);
+cudaError_t launch_tree_attn(const Ctx&, const jt_attn_args& a);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace jt
