@@ -222,6 +222,36 @@ JT_API jt_status jt_tree_accept(const float* target_logits, const int32_t* paren
                          int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes,
                          int32_t* bonus, const jt_exec* exec);
 
+/* ------------------------------------------------------------------------
+ * jt_tree_accept_noalloc — jt_tree_accept for callers that cannot allocate.
+ * The paper has no counterpart: this is a library convenience.
+ *
+ * Same arguments, results and device checks as jt_tree_accept, but the
+ * scratch it needs comes from a fixed array inside the library's device
+ * image instead of exec->workspace (which is ignored). It is meant for
+ * callers that must not call cudaMalloc or any allocating routine — for
+ * example code that runs while a stream is being captured, runtimes whose
+ * device memory is entirely owned by another allocator, or plain C hosts
+ * with no device allocator at hand — so this call allocates nothing.
+ *
+ * Limit: batch * (B + 1) <= 65536; larger requests return
+ * JT_ERR_UNSUPPORTED without launching. The array (256 KiB) lives on every
+ * GPU that loads the library until the process exits.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture that includes this entry point.
+ * Every call on a device shares the one array and it keeps the last call's
+ * contents; nothing in it needs to start at zero (each call writes every
+ * entry it reads before reading it). Calls that overlap on the GPU (on
+ * different streams, or from different host threads without ordering) race
+ * on the array and give undefined results: serialise them.
+ * ------------------------------------------------------------------------ */
+JT_API jt_status jt_tree_accept_noalloc(const float* target_logits, const int32_t* parent,
+                                        const int32_t* token, const int32_t* n_nodes, int batch,
+                                        int B, int n_depth, int vocab, int32_t* acc_len,
+                                        int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus,
+                                        const jt_exec* exec);
+
 #ifdef __cplusplus
 }
 #endif

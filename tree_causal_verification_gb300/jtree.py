@@ -32,7 +32,7 @@ STATUS_NAMES = {0: "JT_OK", 1: "JT_ERR_INVALID_ARG", 2: "JT_ERR_UNSUPPORTED", 3:
 
 EXPORTED = ["jt_status_str", "jt_read_device_error", "jt_topw_workspace_bytes", "jt_topw",
             "jt_tree_expand", "jt_tree_mask", "jt_tree_attn_workspace_bytes", "jt_tree_attn",
-            "jt_tree_accept_workspace_bytes", "jt_tree_accept"]
+            "jt_tree_accept_workspace_bytes", "jt_tree_accept", "jt_tree_accept_noalloc"]
 
 
 class JtError(RuntimeError):
@@ -89,8 +89,9 @@ def load(path: str = LIB_PATH):
             lib.jt_tree_accept_workspace_bytes.argtypes = [_c_int] * 3
             lib.jt_tree_accept.argtypes = [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                            _vp, _vp, _vp, _vp, _pexec]
+            lib.jt_tree_accept_noalloc.argtypes = lib.jt_tree_accept.argtypes
             for name in ("jt_read_device_error", "jt_topw", "jt_tree_expand", "jt_tree_mask",
-                         "jt_tree_attn", "jt_tree_accept"):
+                         "jt_tree_attn", "jt_tree_accept", "jt_tree_accept_noalloc"):
                 getattr(lib, name).restype = _c_int
             _lib = lib
     return _lib
@@ -290,4 +291,30 @@ def jt_tree_accept(target, parent, token, n_nodes, n_depth, out=None, exec=None)
                               n_depth, V, _ptr(out["acc_len"]), _ptr(out["acc_tokens"]),
                               _ptr(out["acc_nodes"]), _ptr(out["bonus"]), ctypes.byref(c)),
            "jt_tree_accept")
+    return out
+
+
+def jt_tree_accept_noalloc(target, parent, token, n_nodes, n_depth, out=None, exec=None):
+    """jt_tree_accept without a workspace: for callers that cannot allocate
+    device scratch. The library uses its own fixed device array instead, so
+    calls on one device must not overlap on the GPU (they share that array).
+    Limit: batch * (B + 1) <= 65536."""
+    batch, B = parent.shape
+    V = target.shape[-1]
+    dev = target.device
+    if out is None:
+        out = dict(acc_len=torch.empty((batch,), dtype=torch.int32, device=dev),
+                   acc_tokens=torch.empty((batch, n_depth), dtype=torch.int32, device=dev),
+                   acc_nodes=torch.empty((batch, n_depth), dtype=torch.int32, device=dev),
+                   bonus=torch.empty((batch,), dtype=torch.int32, device=dev))
+    _need(target, torch.float32, (batch, B + 1, V), "target")
+    _need(parent, torch.int32, (batch, B), "parent")
+    _need(token, torch.int32, (batch, B), "token")
+    _need(n_nodes, torch.int32, (batch,), "n_nodes")
+    c = _exec(exec).c()
+    _check(load().jt_tree_accept_noalloc(_ptr(target), _ptr(parent), _ptr(token), _ptr(n_nodes),
+                                         batch, B, n_depth, V, _ptr(out["acc_len"]),
+                                         _ptr(out["acc_tokens"]), _ptr(out["acc_nodes"]),
+                                         _ptr(out["bonus"]), ctypes.byref(c)),
+           "jt_tree_accept_noalloc")
     return out
