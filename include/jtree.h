@@ -170,7 +170,7 @@ JT_API jt_status jt_tree_mask(const int32_t* parent, const int32_t* n_nodes, int
  *   prefix_len   int32 [batch], n_nodes int32 [batch]
  *   mask         uint32 [batch][B][(B+31)/32] (jt_tree_mask's output)
  *   out          bf16 [batch][B][hq][D]
- *   scale        0 means 1/sqrt(D)
+ *   scale        > 0; 0 means 1/sqrt(D)
  * Limits: D in {64, 128}; hq % hkv == 0; hq/hkv in {1, 2, 4, 8, 16}; 1 <= B <= 256;
  * page_size == 16 when paged. Workspace: jt_tree_attn_workspace_bytes.
  * Device checks: prefix_len beyond max_prefix (or max_pages*page_size), a page

@@ -130,6 +130,7 @@ static jt_status check_attn(const jt_attn_args* a) {
   if (a->batch < 0 || a->B < 1 || a->B > kMaxB || a->hq < 1 || a->hkv < 1 || a->hq % a->hkv)
     return JT_ERR_INVALID_ARG;
   if (a->head_dim != 64 && a->head_dim != 128) return JT_ERR_UNSUPPORTED;
+  if (!(a->scale >= 0.0f)) return JT_ERR_INVALID_ARG;  // negative or NaN
   if (a->hq / a->hkv > 16 || 128 % (a->hq / a->hkv) != 0) return JT_ERR_UNSUPPORTED;
   if (a->batch == 0) return JT_OK;
   if (!a->q || !a->k_tree || !a->v_tree || !a->k_cache || !a->v_cache || !a->prefix_len ||

@@ -9,27 +9,34 @@
 //
 // Kernel design (sm_100 family, tcgen05 + TMA)
 // --------------------------------------------
-// Work unit = (sequence b, KV head kh, M-tile of 128 query rows). Rows are
-// node-major, row = v*g + j, so one unit's 128 rows are 128/g consecutive
-// tree nodes times all g query heads that share KV head kh: every K/V tile
-// streamed from HBM is used by all of them (GQA folded into the MMA M
-// dimension). The unit's keys are the prefix tiles (128 keys each, paged
-// through 16-token pages or contiguous) followed by the tree tiles (only
-// those holding ancestors of the tile's nodes).
+// Rows are node-major, row = v*g + j: 128/g consecutive tree nodes times the
+// g query heads sharing KV head kh make one 128-row M tile, so every K/V
+// tile streamed from HBM serves all of them (GQA folded into MMA M).
+// Work unit = (sequence b, KV head kh, pair of M tiles A and B = 256 rows).
+// The unit's keys are the prefix tiles (128 keys; paged through 16-token
+// pages or contiguous) then the tree tiles holding its nodes' ancestors.
 //
-// One CTA per unit (or per slice of its key tiles when the unit count is too
-// small to fill the GPU: split-KV across a thread-block cluster, merged in
-// distributed shared memory). 192 threads:
-//   warps 0-3  softmax: thread r owns query row r = TMEM lane r. Reads S from
-//              TMEM, applies prefix bound / ancestor bits and the scale,
-//              online softmax in the log2 domain with lazy O rescaling (only
-//              when the row max grows by more than 8, i.e. 2^8), writes P as
-//              bf16 into a 128B-swizzled shared tile;
-//   warp 4     TMA producer: Q once, then K and V tiles into a 2-stage ring;
-//   warp 5     TMEM owner and MMA issuer (one thread):
-//              S[j&1] = Q K_j^T   (M=128, N=128, K=D; S double-buffered)
-//              O     += P_j V_j   (M=128, N=64 per half of D, K=128 keys)
-// TMEM: S0 cols [0,128), S1 [128,256), O [256, 256+D) (512 allocated).
+// One CTA per unit (or per slice of its key tiles when units are too few to
+// fill the GPU: split-KV over a thread-block cluster, merged in distributed
+// shared memory). 320 threads:
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread r of a
+//              warpgroup owns TMEM lane r (= query row). Pass 1 reads S from
+//              TMEM and finds the row max (prefix bound / ancestor bits /
+//              scale applied in registers); pass 2 re-reads S, forms
+//              P = 2^(s - m) and writes it back over S in TMEM as packed bf16.
+//              O is rescaled in TMEM only when a row max grows by more than
+//              2^8 (lazy rescaling; the final 1/l uses the same stale max);
+//   warp 8     TMA producer: Q_A, Q_B once, then K and V into a 2-stage ring;
+//   warp 9     TMEM owner and MMA issuer (one thread), per K/V tile j:
+//              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), where
+//              S_X = Q_X K^T (M=128, N=128, K=D, operands in shared memory)
+//              O_X += P_X V  (M=128, N=64 per half of D, K=128 keys; P from
+//                             TMEM, V from shared memory, MN-major)
+//              so one tile's softmax overlaps the other tile's MMAs. Tensor
+//              ops retire in issue order, so the commit after S_X(j+1) also
+//              certifies that PV_X(j) has finished with P_X / O_X.
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D),
+// O_B [256+D', ...) with D' = 128 for D = 128 (384..511).
 // Every mbarrier wait is bounded; on expiry the CTA raises JT_DEVERR_TIMEOUT,
 // drains its outstanding MMAs, frees TMEM and finishes.
 #include <cooperative_groups.h>
@@ -46,14 +53,16 @@ namespace {
 namespace cg = cooperative_groups;
 using namespace sm100;
 
-constexpr int kThreads = 192;
-constexpr int kTile = 128;                 // query rows per unit = keys per tile
+constexpr int kThreads = 320;
+constexpr int kWarpTMA = 8, kWarpMMA = 9;
+constexpr int kTile = 128;                 // query rows per M tile = keys per K/V tile
+constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitBudget = 4000000000LL;   // ~2 s at 2 GHz
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnParams {
-  int batch, B, hq, hkv, g, npt, n_mtiles, S;
+  int batch, B, hq, hkv, g, npt, n_mpairs, S;
   int paged, max_pages, n_pages, Lbound, words;
   const int32_t* block_table;
   const int32_t* prefix_len;
@@ -65,25 +74,14 @@ struct AttnParams {
 };
 
 struct Bars {
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, drain;
+  uint64_t q_full, kv_full[kStages], kv_empty[kStages], s_full[2], p_full[2], pv_done[2], drain;
   uint32_t tmem_base;
   int abort;
 };
 
-template <int D>
-__device__ __forceinline__ void store_row(const AttnParams& p, int b, int kh, int v, int j,
-                                          const float* o, float inv) {
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * p.g + j) * D);
-#pragma unroll
-  for (int u = 0; u < D / 8; ++u) {
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __nv_bfloat162 two = __floats2bfloat162_rn(o[8 * u + 2 * e] * inv, o[8 * u + 2 * e + 1] * inv);
-      w[e] = *reinterpret_cast<uint32_t*>(&two);
-    }
-    dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 two = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&two);
 }
 
 template <int D>
@@ -93,28 +91,27 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                     const __grid_constant__ CUtensorMap mvt, const AttnParams p) {
   constexpr int CH = D / 64;               // 64-element (128-byte) chunks of the head dim
   constexpr int QB = kTile * D * 2;        // bytes of one Q, K or V tile
-  constexpr int PB = kTile * kTile * 2;    // bytes of the P tile
-  constexpr uint32_t kTxKV = 2 * QB;
+  constexpr int CHB = kTile * 128;         // bytes of one 64-column chunk of a tile
   constexpr int KS = 4 * CH;               // K=16 steps of Q K^T
+  constexpr int OSTRIDE = D == 128 ? 128 : 64;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = sm;
-  uint8_t* sP = sm + 5 * QB;
-  Bars* bars = reinterpret_cast<Bars*>(sm + 5 * QB + PB);
-  auto sK = [&](int st) { return sm + QB + st * 2 * QB; };
-  auto sV = [&](int st) { return sm + 2 * QB + st * 2 * QB; };
+  Bars* bars = reinterpret_cast<Bars*>(sm + 2 * QB + kStages * 2 * QB);
+  auto sQ = [&](int X) { return sm + X * QB; };
+  auto sK = [&](int st) { return sm + 2 * QB + st * 2 * QB; };
+  auto sV = [&](int st) { return sm + 3 * QB + st * 2 * QB; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
   const int rank = (int)(blockIdx.x % (unsigned)S);
   const int unit = (int)(blockIdx.x / (unsigned)S);
-  const int mt = unit % p.n_mtiles;
-  const int bk = unit / p.n_mtiles;
+  const int mp = unit % p.n_mpairs;
+  const int bk = unit / p.n_mpairs;
   const int kh = bk % p.hkv, b = bk / p.hkv;
   const int g = p.g, npt = p.npt;
-  const int v0 = mt * npt;
+  const int v0 = mp * 2 * npt;
 
   // ---- validate the sequence (same verdict in every CTA of the sequence) ----
   const int n_raw = p.n_nodes[b];
@@ -134,8 +131,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int n = bad ? 0 : n_raw;
 
   const bool has_rows = v0 < n;
+  const bool twoB = v0 + npt < n;          // tile B holds at least one live node
   const int p_tiles = has_rows ? (L + kTile - 1) / kTile : 0;
-  const int v_last = min(v0 + npt, n) - 1;
+  const int v_last = min(v0 + 2 * npt, n) - 1;
   const int t_tree = has_rows ? (v_last + kTile) / kTile : 0;
   const int t_tot = p_tiles + t_tree;
   const int t_begin = (int)((long)rank * t_tot / S);
@@ -143,9 +141,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int T = t_end - t_begin;
 
   if (!has_rows) {
-    // Every row of this unit belongs to an unused budget slot: zeros. The
-    // cluster's CTAs split the rows; no CTA of the cluster touches DSMEM.
-    const int R = kTile / S;
+    // Every row of this unit is an unused budget slot: zeros. The cluster's
+    // CTAs split the rows; no CTA of the cluster touches DSMEM.
+    const int R = 2 * kTile / S;
     for (int i = tid; i < R * (D / 8); i += kThreads) {
       const int r = rank * R + i / (D / 8), u = i % (D / 8);
       const int v = v0 + r / g, j = r % g;
@@ -159,19 +157,20 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   // ---- set-up: barriers, TMEM ----
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], 4);
     }
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->pv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 4);
+      mbar_init(&bars->pv_done[i], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMMA) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -188,16 +187,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
     return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort, kWaitBudget)) != 0;
   };
-
   // Valid keys of tile t (prefix tiles first, then tree tiles).
   auto tile_valid = [&](int t) {
     return t < p_tiles ? min(kTile, L - t * kTile) : min(kTile, n - (t - p_tiles) * kTile);
   };
 
-  float o_acc[D];
-  float m_run = -INFINITY, l_run = 0.0f;
-
-  if (warp == 4) {
+  if (warp == kWarpTMA) {
     // =================== TMA producer ===================
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&mq);
@@ -205,18 +200,20 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       tma_prefetch_desc(&mvc);
       tma_prefetch_desc(&mkt);
       tma_prefetch_desc(&mvt);
-      mbar_arrive_expect_tx(&bars->q_full, QB);
+      mbar_arrive_expect_tx(&bars->q_full, (twoB ? 2 : 1) * QB);
+      for (int X = 0; X < (twoB ? 2 : 1); ++X)
 #pragma unroll
-      for (int ch = 0; ch < CH; ++ch)
-        tma_load_4d(sQ + ch * (kTile * 128), &mq, &bars->q_full, ch * 64, kh * g, v0, b);
+        for (int ch = 0; ch < CH; ++ch)
+          tma_load_4d(sQ(X) + ch * CHB, &mq, &bars->q_full, ch * 64, kh * g, v0 + X * npt, b);
       const int np = (L + kPageSize - 1) / kPageSize;
       for (int jt = 0; jt < T; ++jt) {
-        const int t = t_begin + jt, st = jt & 1;
-        if (jt >= 2 && !mbar_wait(&bars->kv_empty[st], ((jt >> 1) + 1) & 1, abort, kWaitBudget)) {
+        const int t = t_begin + jt, st = jt % kStages;
+        if (jt >= kStages &&
+            !mbar_wait(&bars->kv_empty[st], ((jt / kStages) + 1) & 1, abort, kWaitBudget)) {
           fail();
           break;
         }
-        mbar_arrive_expect_tx(&bars->kv_full[st], kTxKV);
+        mbar_arrive_expect_tx(&bars->kv_full[st], 2 * QB);
         uint8_t* dk = sK(st);
         uint8_t* dv = sV(st);
         if (t < p_tiles) {
@@ -228,155 +225,173 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
               const int page = pi < np ? p.block_table[(size_t)b * p.max_pages + pi] : 0;
 #pragma unroll
               for (int ch = 0; ch < CH; ++ch) {
-                tma_load_4d(dk + ch * (kTile * 128) + pg * (kPageSize * 128), &mkc,
-                            &bars->kv_full[st], ch * 64, kh, 0, page);
-                tma_load_4d(dv + ch * (kTile * 128) + pg * (kPageSize * 128), &mvc,
-                            &bars->kv_full[st], ch * 64, kh, 0, page);
+                tma_load_4d(dk + ch * CHB + pg * (kPageSize * 128), &mkc, &bars->kv_full[st],
+                            ch * 64, kh, 0, page);
+                tma_load_4d(dv + ch * CHB + pg * (kPageSize * 128), &mvc, &bars->kv_full[st],
+                            ch * 64, kh, 0, page);
               }
             }
           } else {
 #pragma unroll
             for (int ch = 0; ch < CH; ++ch) {
-              tma_load_4d(dk + ch * (kTile * 128), &mkc, &bars->kv_full[st], ch * 64, kh, key0, b);
-              tma_load_4d(dv + ch * (kTile * 128), &mvc, &bars->kv_full[st], ch * 64, kh, key0, b);
+              tma_load_4d(dk + ch * CHB, &mkc, &bars->kv_full[st], ch * 64, kh, key0, b);
+              tma_load_4d(dv + ch * CHB, &mvc, &bars->kv_full[st], ch * 64, kh, key0, b);
             }
           }
         } else {
           const int u0 = (t - p_tiles) * kTile;
 #pragma unroll
           for (int ch = 0; ch < CH; ++ch) {
-            tma_load_4d(dk + ch * (kTile * 128), &mkt, &bars->kv_full[st], ch * 64, kh, u0, b);
-            tma_load_4d(dv + ch * (kTile * 128), &mvt, &bars->kv_full[st], ch * 64, kh, u0, b);
+            tma_load_4d(dk + ch * CHB, &mkt, &bars->kv_full[st], ch * 64, kh, u0, b);
+            tma_load_4d(dv + ch * CHB, &mvt, &bars->kv_full[st], ch * 64, kh, u0, b);
           }
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMMA) {
     // =================== MMA issuer ===================
     constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t id_o = idesc_bf16(128, 64, 0, 1);
-    const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
-    auto issue_pv = [&](int jt) {
-      const uint32_t v_addr = smem_u32(sV(jt & 1));
+    auto issue_s = [&](int X, int st) {
+      const uint32_t q_addr = smem_u32(sQ(X)), k_addr = smem_u32(sK(st));
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const uint32_t off = (kk >> 2) * CHB + (kk & 3) * 32;
+        mma_bf16_ss(tmem + X * 128, sdesc_sw128(q_addr + off, 16, 1024),
+                    sdesc_sw128(k_addr + off, 16, 1024), id_s, kk > 0);
+      }
+      mma_commit(&bars->s_full[X]);
+    };
+    auto issue_pv = [&](int X, int jt) {
+      const uint32_t v_addr = smem_u32(sV(jt % kStages));
 #pragma unroll
       for (int h = 0; h < CH; ++h)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          const uint32_t boff = h * (kTile * 128) + kk * 2048;
-          mma_bf16_ss(tmem + 256 + 64 * h, sdesc_sw128(p_addr + aoff, 16, 1024),
-                      sdesc_sw128(v_addr + boff, kTile * 128, 1024), id_o, jt > 0 || kk > 0);
-        }
-      mma_commit(&bars->kv_empty[jt & 1]);
-      mma_commit(&bars->pv_done);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + 256 + X * OSTRIDE + 64 * h, tmem + X * 128 + kk * 8,
+                      sdesc_sw128(v_addr + h * CHB + kk * 2048, CHB, 1024), id_o,
+                      jt > 0 || kk > 0);
+      mma_commit(&bars->pv_done[X]);
     };
-    bool ok = T > 0 && warp_wait(&bars->q_full, 0);
-    if (T > 0 && !ok) fail();
-    for (int jt = 0; ok && jt < T; ++jt) {
-      const int st = jt & 1;
-      if (!warp_wait(&bars->kv_full[st], (jt >> 1) & 1)) { fail(); ok = false; break; }
-      // Rows of V past the tile's valid keys may hold anything (NaN included);
-      // P is 0 there, but 0 * NaN is NaN, so zero them before P V reads them.
+    // Rows of V past a tile's valid keys may hold anything (NaN included); P
+    // is 0 there but 0 * NaN is NaN, so they are zeroed before P V reads them.
+    auto zero_v_tail = [&](int jt) {
       const int valid = tile_valid(t_begin + jt);
       if (valid < kTile) {
-        uint8_t* vt = sV(st);
+        uint8_t* vt = sV(jt % kStages);
         for (int i = lane; i < (kTile - valid) * CH * 8; i += 32) {
           const int r = valid + i / (CH * 8), rem = i % (CH * 8);
-          const int ch = rem / 8, u = rem % 8;
-          *reinterpret_cast<uint4*>(vt + ch * (kTile * 128) + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vt + (rem / 8) * CHB + r * 128 + (rem % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (jt >= 2 && !warp_wait(&bars->s_free[st], ((jt >> 1) + 1) & 1)) {
-        fail(); ok = false; break;
-      }
+    };
+    bool ok = T > 0 && warp_wait(&bars->q_full, 0) && warp_wait(&bars->kv_full[0], 0);
+    if (T > 0 && !ok) fail();
+    if (ok) {
+      zero_v_tail(0);
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t k_addr = smem_u32(sK(st));
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + st * 128, sdesc_sw128(q_addr + off, 16, 1024),
-                      sdesc_sw128(k_addr + off, 16, 1024), id_s, kk > 0);
-        }
-        mma_commit(&bars->s_full[st]);
+        issue_s(0, 0);
+        if (twoB) issue_s(1, 0);
       }
       __syncwarp();
-      if (jt >= 1) {
-        if (!warp_wait(&bars->p_full, (jt - 1) & 1)) { fail(); ok = false; break; }
+    }
+    for (int jt = 0; ok && jt < T; ++jt) {
+      const int st = jt % kStages;
+      if (!warp_wait(&bars->p_full[0], jt & 1)) { fail(); ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) issue_pv(0, jt);
+      __syncwarp();
+      const bool more = jt + 1 < T;
+      if (more) {
+        const int st1 = (jt + 1) % kStages;
+        if (!warp_wait(&bars->kv_full[st1], ((jt + 1) / kStages) & 1)) { fail(); ok = false; break; }
+        zero_v_tail(jt + 1);
         tc_fence_after();
-        if (lane == 0) issue_pv(jt - 1);
+        if (lane == 0) issue_s(0, st1);
         __syncwarp();
       }
-    }
-    if (ok) {
-      if (warp_wait(&bars->p_full, (T - 1) & 1)) {
+      if (twoB) {
+        if (!warp_wait(&bars->p_full[1], jt & 1)) { fail(); ok = false; break; }
         tc_fence_after();
-        if (lane == 0) issue_pv(T - 1);
+        if (lane == 0) issue_pv(1, jt);
         __syncwarp();
-      } else {
-        fail();
       }
+      if (lane == 0) {
+        mma_commit(&bars->kv_empty[st]);
+        if (twoB && more) issue_s(1, (jt + 1) % kStages);
+      }
+      __syncwarp();
     }
-  } else {
-    // =================== softmax (warps 0-3) ===================
-    const int r = tid;
-    const int v = v0 + r / g;
+  }
+
+  // =================== softmax (warps 0-7, tile X = warp / 4) ===================
+  float m_run = -INFINITY, l_run = 0.0f;
+  const int X = warp >> 2;
+  const int r = tid & 127;
+  const int R = X * kTile + r;              // row within the unit's 256
+  const int v = v0 + R / g;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t s_col = tmem + lane_base + X * 128;
+  const uint32_t o_col = tmem + lane_base + 256 + X * OSTRIDE;
+  const bool tile_live = X == 0 || twoB;
+  bool sm_ok = true;
+  if (warp < 8 && tile_live) {
     const bool row_valid = v < n;
     uint32_t mrow[kMaxWords];
 #pragma unroll
     for (int w = 0; w < kMaxWords; ++w)
       mrow[w] = (row_valid && w < p.words) ? p.mask[((size_t)b * p.B + v) * p.words + w] : 0u;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint8_t* prow = sP + r * 128;
-    const int rsw = r & 7;
-    bool ok = true;
     for (int jt = 0; jt < T; ++jt) {
-      const int t = t_begin + jt, sb = jt & 1;
-      if (!warp_wait(&bars->s_full[sb], (jt >> 1) & 1)) { fail(); ok = false; break; }
+      const int t = t_begin + jt;
+      if (!warp_wait(&bars->s_full[X], jt & 1)) { fail(); sm_ok = false; break; }
       tc_fence_after();
-      float x[kTile];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float tmp[32];
-        tmem_ld32(tmem + lane_base + sb * 128 + c * 32, tmp);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c * 32 + i] = tmp[i];
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free[sb]);
-      // Mask and scale into the log2 domain.
+      // Which keys of this tile the row sees: c < lim, and for tree tiles the
+      // ancestor bit of key u0 + c.
+      const bool tree = t >= p_tiles;
+      const int lim = tree ? n - (t - p_tiles) * kTile : L - t * kTile;
+      const bool hi = tree && ((t - p_tiles) * kTile) >= 128;
+      const uint32_t ws0 = tree ? (hi ? mrow[4] : mrow[0]) : 0xFFFFFFFFu;
+      const uint32_t ws1 = tree ? (hi ? mrow[5] : mrow[1]) : 0xFFFFFFFFu;
+      const uint32_t ws2 = tree ? (hi ? mrow[6] : mrow[2]) : 0xFFFFFFFFu;
+      const uint32_t ws3 = tree ? (hi ? mrow[7] : mrow[3]) : 0xFFFFFFFFu;
+      auto word_of = [&](int c) {   // ancestor bits of keys 32c..32c+31 of this tile
+        const uint32_t w01 = (c & 1) ? ws1 : ws0, w23 = (c & 1) ? ws3 : ws2;
+        return (c & 2) ? w23 : w01;
+      };
+      // Pass 1: row max of the visible scores. A prefix tile whose 128 keys
+      // are all visible needs no per-key test (the common case by far).
+      const bool full = !tree && lim >= kTile;
       float tmax = -INFINITY;
-      if (t < p_tiles) {
-        const int kv = L - t * kTile;
+      if (full) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tmem_ld32(s_col + c * 32, x);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          x[c] = (c < kv) ? x[c] * sl2 : -INFINITY;
-          tmax = fmaxf(tmax, x[c]);
+          for (int i = 0; i < 32; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
         }
+        tmax *= sl2;   // sl2 > 0
       } else {
-        const int u0 = (t - p_tiles) * kTile;
-        const int wb = u0 >> 5;
-        uint32_t wsel[4];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tmem_ld32(s_col + c * 32, x);
+          tmem_wait_ld();
+          const uint32_t wc = word_of(c);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) wsel[i] = (wb == 0) ? mrow[i] : mrow[4 + i];
-        const int ncap = n - u0;
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          const bool vis = ((wsel[c >> 5] >> (c & 31)) & 1u) && c < ncap;
-          x[c] = vis ? x[c] * sl2 : -INFINITY;
-          tmax = fmaxf(tmax, x[c]);
+          for (int i = 0; i < 32; ++i) {
+            const bool vis = ((wc >> i) & 1u) && (c * 32 + i) < lim;
+            tmax = fmaxf(tmax, vis ? x[i] * sl2 : -INFINITY);
+          }
         }
       }
       const float mnew = fmaxf(m_run, tmax);
-      if (jt >= 1) {
-        if (!warp_wait(&bars->pv_done, (jt - 1) & 1)) { fail(); ok = false; break; }
-        tc_fence_after();
-      }
       const bool need = mnew > m_run + kRescaleLog2;
       float corr = 1.0f;
       if (need) {
@@ -385,69 +400,126 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         m_run = mnew;
       }
       if (jt >= 1 && __any_sync(0xFFFFFFFFu, need)) {
+        // PV_X(jt-1) is complete: the commit behind s_full covers it.
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          float tmp[32];
-          tmem_ld32(tmem + lane_base + 256 + c * 32, tmp);
+          float o[32];
+          tmem_ld32(o_col + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) tmp[i] *= corr;
-          tmem_st32(tmem + lane_base + 256 + c * 32, tmp);
+          for (int i = 0; i < 32; ++i) o[i] *= corr;
+          tmem_st32(o_col + c * 32, o);
         }
-        tmem_wait_st();
       }
+      // Pass 2: P = 2^(s - m) as bf16 pairs over the S columns already read.
       const float muse = (m_run == -INFINITY) ? 0.0f : m_run;
       float lsum = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float x[32];
+        tmem_ld32(s_col + c * 32, x);
+        tmem_wait_ld();
+        uint32_t pk[16];
+        if (full) {
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = ch * 64 + u * 8 + 2 * e;
-            const float p0 = ex2(x[c] - muse), p1 = ex2(x[c + 1] - muse);
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(x[2 * i], sl2, -muse));
+            const float p1 = ex2(fmaf(x[2 * i + 1], sl2, -muse));
             lsum += p0 + p1;
-            __nv_bfloat162 two = __floats2bfloat162_rn(p0, p1);
-            w[e] = *reinterpret_cast<uint32_t*>(&two);
+            pk[i] = pack_bf16(p0, p1);
           }
-          *reinterpret_cast<uint4*>(prow + ch * (kTile * 128) + ((u ^ rsw) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+          const uint32_t wc = word_of(c);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int i0 = 2 * i, i1 = 2 * i + 1;
+            const bool v0ok = ((wc >> i0) & 1u) && (c * 32 + i0) < lim;
+            const bool v1ok = ((wc >> i1) & 1u) && (c * 32 + i1) < lim;
+            const float p0 = v0ok ? ex2(fmaf(x[i0], sl2, -muse)) : 0.0f;
+            const float p1 = v1ok ? ex2(fmaf(x[i1], sl2, -muse)) : 0.0f;
+            lsum += p0 + p1;
+            pk[i] = pack_bf16(p0, p1);
+          }
         }
+        tmem_st16(s_col + c * 16, pk);
       }
+      tmem_wait_st();
       l_run += lsum;
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);
+      if (lane == 0) mbar_arrive(&bars->p_full[X]);
     }
-    // Final accumulator.
-    if (ok && T > 0 && warp_wait(&bars->pv_done, (T - 1) & 1)) {
-      tc_fence_after();
+    if (sm_ok && T > 0) {
+      if (warp_wait(&bars->pv_done[X], (T - 1) & 1)) tc_fence_after();
+      else { fail(); sm_ok = false; }
+    }
+  }
+  const bool have_o = warp < 8 && tile_live && sm_ok && T > 0;
+  if (!have_o) { m_run = -INFINITY; l_run = 0.0f; }
+  // Every live tile has seen its last P V complete, so the tensor pipe and
+  // the K/V ring are idle from here on: the merge buffer may overlay them.
+  __syncthreads();
+
+  // ---- output (S == 1) or publish partials (S > 1); both read O from TMEM ----
+  float* o_s = reinterpret_cast<float*>(sm);                // [D/4][256] float4s over Q and the K/V ring
+  float* m_s = o_s + 2 * kTile * D;
+  float* l_s = m_s + 2 * kTile;
+  float* fac = l_s + 2 * kTile;                             // [256 / S][S]
+  if (warp < 8) {
+    const int j = R % g;
+    const bool write_row = v < p.B;
+    const float inv = (v < n && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+    if (S > 1) {
+      // The K/V ring and Q are dead: every PV has completed.
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        float tmp[32];
-        tmem_ld32(tmem + lane_base + 256 + c * 32, tmp);
+        float o[32];
+        if (have_o) {
+          tmem_ld32(o_col + c * 32, o);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o_acc[c * 32 + i] = tmp[i];
+          for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+        }
+        // float4-column-major ([D/4][256]): consecutive rows hit consecutive banks.
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          reinterpret_cast<float4*>(o_s)[(c * 8 + i / 4) * (2 * kTile) + R] =
+              make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
       }
-      tmem_wait_ld();
+      m_s[R] = m_run;
+      l_s[R] = l_run;
     } else {
-      if (ok && T > 0) fail();
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * g + j) * D);
 #pragma unroll
-      for (int i = 0; i < D; ++i) o_acc[i] = 0.0f;
-      if (T == 0) { m_run = -INFINITY; l_run = 0.0f; }
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (have_o) {
+          tmem_ld32(o_col + c * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+        }
+        if (write_row) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[c * 4 + q] = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                        pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                        pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                        pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+        }
+      }
     }
   }
 
   // ---- release TMEM (after draining outstanding MMAs on the abort path) ----
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMMA) {
     tc_fence_after();
     if (*abort && lane == 0) {
       mma_commit(&bars->drain);
-      mbar_try_wait(&bars->drain, 0);
       const long long t0 = clock64();
       while (!mbar_try_wait(&bars->drain, 0) && clock64() - t0 < kWaitBudget) {
       }
@@ -455,72 +527,47 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (S == 1) return;
 
-  // ---- output ----
-  if (S == 1) {
-    if (tid < kTile) {
-      const int r = tid, v = v0 + r / g, jh = r % g;
-      if (v < p.B) store_row<D>(p, b, kh, v, jh, o_acc, (v < n && l_run > 0.0f) ? 1.0f / l_run : 0.0f);
-    }
-    return;
-  }
-  // Split-KV: publish (O, m, l) of every row in shared memory, then rank k
-  // merges rows [k*R, (k+1)*R) across the cluster through DSMEM.
-  float* o_s = reinterpret_cast<float*>(sm + QB);          // [128][D], over the K/V ring
-  float* m_s = o_s + kTile * D;
-  float* l_s = m_s + kTile;
-  float* fac = l_s + kTile;                                 // [R][S] = 128 floats
-  if (tid < kTile) {
-#pragma unroll
-    for (int i = 0; i < D; i += 4)
-      *reinterpret_cast<float4*>(o_s + tid * D + i) =
-          make_float4(o_acc[i], o_acc[i + 1], o_acc[i + 2], o_acc[i + 3]);
-    m_s[tid] = m_run;
-    l_s[tid] = l_run;
-  }
+  // ---- split-KV merge: rank k finishes rows [k*RR, (k+1)*RR) of the 256 ----
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  const int R = kTile / S;
-  if (tid < R) {
-    const int row = rank * R + tid;
+  const int RR = 2 * kTile / S;
+  if (tid < RR) {
+    const int row = rank * RR + tid;
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, cluster.map_shared_rank(m_s, s)[row]);
+    for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, cluster.map_shared_rank(m_s, s2)[row]);
     float lsum = 0.0f;
-    for (int s = 0; s < S; ++s) {
-      const float ms = cluster.map_shared_rank(m_s, s)[row];
+    for (int s2 = 0; s2 < S; ++s2) {
+      const float ms = cluster.map_shared_rank(m_s, s2)[row];
       const float f = (ms == -INFINITY) ? 0.0f : ex2(ms - M);
-      fac[tid * S + s] = f;
-      lsum += f * cluster.map_shared_rank(l_s, s)[row];
+      fac[tid * S + s2] = f;
+      lsum += f * cluster.map_shared_rank(l_s, s2)[row];
     }
     const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-    for (int s = 0; s < S; ++s) fac[tid * S + s] *= inv;
+    for (int s2 = 0; s2 < S; ++s2) fac[tid * S + s2] *= inv;
   }
   __syncthreads();
-  for (int i = tid; i < R * (D / 8); i += kThreads) {
+  for (int i = tid; i < RR * (D / 8); i += kThreads) {
     const int rl = i / (D / 8), u = i % (D / 8);
-    const int row = rank * R + rl;
-    const int v = v0 + row / g, jh = row % g;
-    if (v >= p.B) continue;
+    const int row = rank * RR + rl;
+    const int vv = v0 + row / g, jh = row % g;
+    if (vv >= p.B) continue;
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-    if (v < n) {
-      for (int s = 0; s < S; ++s) {
-        const float f = fac[rl * S + s];
-        const float4* src = reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s, s) + row * D + u * 8);
-        const float4 a = src[0], c4 = src[1];
+    if (vv < n) {
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float f = fac[rl * S + s2];
+        const float4* src = reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s, s2));
+        const float4 a = src[(2 * u) * (2 * kTile) + row], c4 = src[(2 * u + 1) * (2 * kTile) + row];
         acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
         acc[4] += f * c4.x; acc[5] += f * c4.y; acc[6] += f * c4.z; acc[7] += f * c4.w;
       }
     }
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __nv_bfloat162 two = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
-      w[e] = *reinterpret_cast<uint32_t*>(&two);
-    }
-    reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * g + jh) * D)[u] =
-        make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[u] =
+        make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                   pack_bf16(acc[6], acc[7]));
   }
   cluster.sync();  // keep this CTA's shared memory alive until every rank has read it
 }
@@ -564,7 +611,7 @@ bool make_map(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
 }
 
 template <int D>
-size_t smem_bytes() { return 5 * (size_t)kTile * D * 2 + (size_t)kTile * kTile * 2 + 256 + 1024; }
+size_t smem_bytes() { return (2 + 2 * kStages) * (size_t)kTile * D * 2 + 256 + 1024; }
 
 template <int D>
 cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
@@ -575,10 +622,11 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
 
-  const int units = a.batch * a.hkv * p.n_mtiles;
+  const int units = a.batch * a.hkv * p.n_mpairs;
   const int tiles_max = (p.Lbound + kTile - 1) / kTile + (a.B + kTile - 1) / kTile;
+  // Split the key tiles over a cluster only while every cluster of the grid
+  // can be resident at once (one wave) and the grid stays within the SMs.
   int S = 1;
-  while (S < 16 && units * S * 2 <= c.num_sms && S * 2 <= tiles_max) S *= 2;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -590,14 +638,17 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  while (S > 1) {  // largest split the hardware can co-schedule as a cluster
-    attr[0].val.clusterDim.x = S;
-    cfg.gridDim = dim3(units * S);
+  for (int cand = 2; cand <= 8; cand *= 2) {
+    if (units * cand > c.num_sms || cand > tiles_max) break;
+    attr[0].val.clusterDim.x = cand;
+    cfg.gridDim = dim3(units * cand);
     int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) == cudaSuccess && nclusters > 0)
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
       break;
-    cudaGetLastError();
-    S >>= 1;
+    }
+    if (nclusters < units) break;
+    S = cand;
   }
   p.S = S;
   attr[0].val.clusterDim.x = S;
@@ -646,7 +697,7 @@ cudaError_t launch_tree_attn(const Ctx& c, const jt_attn_args& a) {
   p.hkv = a.hkv;
   p.g = a.hq / a.hkv;
   p.npt = kTile / p.g;
-  p.n_mtiles = (a.B + p.npt - 1) / p.npt;
+  p.n_mpairs = ((a.B + p.npt - 1) / p.npt + 1) / 2;
   p.paged = a.block_table != nullptr;
   p.max_pages = a.max_pages;
   p.n_pages = a.n_pages;

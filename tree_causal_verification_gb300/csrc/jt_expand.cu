@@ -16,7 +16,9 @@
 // key (ties -> lower id, as the heap order requires). The W children of a
 // pop are created by W lanes at once; each is handed to its owner lane by a
 // shuffle. Scores are binary32 sums (__fadd_rn), the same adds as the
-// definition.
+// definition. The sequence's N x W candidates are staged in shared memory
+// first, so no pop waits on a global load (the depth that selects the next
+// candidate row is only known once the pop is done).
 #include <climits>
 
 #include "jt_internal.cuh"
@@ -33,14 +35,21 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
                    int32_t* __restrict__ token_o, int32_t* __restrict__ depth_o,
                    float* __restrict__ score_o, int32_t* __restrict__ n_nodes_o) {
   __shared__ uint8_t depth_s[kWarpsPerBlock][kMaxB];
+  extern __shared__ int32_t cand_s[];   // per warp: N*W tokens then N*W log-probs
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kWarpsPerBlock + warp;
+  const int b = blockIdx.x * (blockDim.x >> 5) + warp;
   if (b >= batch) return;  // whole warp leaves together
   constexpr unsigned kFull = 0xFFFFFFFFu;
 
-  const int32_t* tk = tok + (size_t)b * N * W;
-  const float* lp = logp + (size_t)b * N * W;
+  const int nw = N * W;
+  int32_t* tk = cand_s + (size_t)warp * 2 * nw;
+  float* lp = reinterpret_cast<float*>(tk + nw);
+  for (int i = lane; i < nw; i += 32) {
+    tk[i] = __ldg(tok + (size_t)b * nw + i);
+    lp[i] = __ldg(logp + (size_t)b * nw + i);
+  }
+  __syncwarp();
   int32_t* par = parent_o + (size_t)b * B;
   int32_t* tko = token_o + (size_t)b * B;
   int32_t* dpo = depth_o + (size_t)b * B;
@@ -62,8 +71,8 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
     float csc = 0.0f;
     if (lane < nc) {                       // lane r creates child r
       const int v = count + lane;
-      const int t = __ldg(tk + (d - 1) * W + lane);
-      csc = __fadd_rn(cur_s, __ldg(lp + (d - 1) * W + lane));
+      const int t = tk[(d - 1) * W + lane];
+      csc = __fadd_rn(cur_s, lp[(d - 1) * W + lane]);
       par[v] = cur;
       tko[v] = t;
       dpo[v] = d;
@@ -121,10 +130,13 @@ cudaError_t launch_tree_expand(const Ctx& c, const int32_t* tok, const float* lo
                                int32_t* depth, float* score, int32_t* n_nodes) {
   if (batch == 0) return cudaSuccess;
   const int slots = (B + 31) / 32;
-  dim3 grid((batch + kWarpsPerBlock - 1) / kWarpsPerBlock), block(kWarpsPerBlock * 32);
-#define JT_EXPAND(S)                                                                       \
-  tree_expand_kernel<S><<<grid, block, 0, c.stream>>>(tok, logp, batch, n_depth, W, B,     \
-                                                       parent, token, depth, score, n_nodes)
+  // Candidates staged per warp: 8 bytes each, at most 64 x 32 (16 KiB).
+  const int warps = (size_t)n_depth * W * 8 * kWarpsPerBlock <= 44 * 1024 ? kWarpsPerBlock : 1;
+  const size_t smem = (size_t)warps * n_depth * W * 8;
+  dim3 grid((batch + warps - 1) / warps), block(warps * 32);
+#define JT_EXPAND(S)                                                                        \
+  tree_expand_kernel<S><<<grid, block, smem, c.stream>>>(tok, logp, batch, n_depth, W, B,   \
+                                                          parent, token, depth, score, n_nodes)
   if (slots <= 1) JT_EXPAND(1);
   else if (slots <= 2) JT_EXPAND(2);
   else if (slots <= 4) JT_EXPAND(4);
