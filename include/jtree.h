@@ -213,10 +213,12 @@ JT_API jt_status jt_tree_attn(const jt_attn_args* args, const jt_exec* exec);
  *   bonus      int32 [batch]            the last argmax (committed too)
  * Committed tokens this step = acc_len + 1.
  * Limits: 1 <= B <= 256, 1 <= n_depth <= 64, vocab % 4 == 0.
- * Workspace: jt_tree_accept_workspace_bytes. Device checks: bad parent, token
+ * Workspace: jt_tree_accept_workspace_bytes (0 when the tree is much wider
+ * than a root path, (B+1) > 4(N+1): then only path rows are read, one
+ * thread-block cluster per sequence). Device checks: bad parent, token
  * or n_nodes set a flag and give acc_len 0, bonus -1 for that sequence.
  * ------------------------------------------------------------------------ */
-JT_API size_t jt_tree_accept_workspace_bytes(int batch, int B, int vocab);
+JT_API size_t jt_tree_accept_workspace_bytes(int batch, int B, int n_depth, int vocab);
 JT_API jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, const int32_t* token,
                          const int32_t* n_nodes, int batch, int B, int n_depth, int vocab,
                          int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes,
@@ -227,7 +229,8 @@ JT_API jt_status jt_tree_accept(const float* target_logits, const int32_t* paren
  * The paper has no counterpart: this is a library convenience.
  *
  * Same arguments, results and device checks as jt_tree_accept, but the
- * scratch it needs comes from a fixed array inside the library's device
+ * scratch it needs (per-row argmaxes, for chains and trees not much wider
+ * than a root path) comes from a fixed array inside the library's device
  * image instead of exec->workspace (which is ignored). It is meant for
  * callers that must not call cudaMalloc or any allocating routine — for
  * example code that runs while a stream is being captured, runtimes whose

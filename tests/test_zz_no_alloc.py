@@ -41,9 +41,12 @@ def make_case(seed, batch, N, W, B, V):
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
     torch.cuda.set_device(0)
     ex = jtree.Exec(DEV)
-    # Two different shapes in a row: the second call reuses (and must not be
-    # confused by) what the first left in the shared array.
-    for seed, shape in ((1, (16, 16, 4, 128, 2048)), (2, (5, 8, 2, 64, 151936))):
+    # Two different shapes in a row that both keep per-row argmaxes in the
+    # library's array (chains and trees not much wider than a root path): the
+    # second call reuses, and must not be confused by, what the first left
+    # there. A third, wide tree walks the path and needs no array at all.
+    for seed, shape in ((1, (12, 16, 1, 16, 4096)), (2, (5, 8, 2, 24, 151936)),
+                        (3, (16, 16, 4, 128, 2048))):
         args = make_case(seed, *shape)
         want = jtree.jt_tree_accept(*args, exec=ex)
         got = jtree.jt_tree_accept_noalloc(*args, exec=ex)

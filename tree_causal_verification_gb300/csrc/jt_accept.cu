@@ -6,12 +6,20 @@
 // paper.rainbus.top, "前置知识"; JetSpec++ summary on paperlayer.ai, §3
 // "Preliminaries"). Argmax ties go to the lowest token id.
 //
-// Two launches:
-//  1. argmax of every live target row (row 0 and rows 1+v, v < n_nodes), one
-//     HBM pass with the same clustered row scan as jt_topw (K = 1, no
-//     log-sum-exp); the per-row argmax goes to the workspace;
-//  2. the walk: one warp per sequence, each step a warp-wide search for the
-//     child whose token matches (__reduce_min_sync picks the lowest id).
+// Two strategies, chosen per call from the shape:
+//  * path walk (trees much larger than one root path, (B+1) > 4(N+1)): one
+//    thread-block cluster per sequence walks down the tree. At each level
+//    every CTA scans its segment of the current node's target row, the CTAs
+//    exchange (max, index) partials through distributed shared memory, and
+//    each CTA finds the matching child itself. Only the rows on the accepted
+//    path (at most N+1 per sequence) are read. When the batch is small, the
+//    rows of the current node's children are prefetched into L2 while the
+//    current row is scanned, hiding the next level's DRAM latency.
+//  * all rows (chains and small trees, where nearly every row may be on the
+//    path): (1) argmax of every live target row with the clustered row scan
+//    of jt_topw (K = 1, no log-sum-exp) into the workspace, then (2) one warp
+//    per sequence walks, each step a warp-wide search for the matching child
+//    (__reduce_min_sync picks the lowest id).
 #include "jt_rowscan.cuh"
 
 namespace jt {
@@ -98,10 +106,138 @@ accept_walk_kernel(const int32_t* __restrict__ am, const int32_t* __restrict__ p
   }
 }
 
+constexpr int kPathThreads = 256;
+
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+struct ArgPart {
+  float v;
+  int i;
+};
+
+__global__ void __launch_bounds__(kPathThreads)
+accept_path_kernel(const float* __restrict__ target, const int32_t* __restrict__ parent,
+                   const int32_t* __restrict__ token, const int32_t* __restrict__ n_nodes, int B,
+                   int N, int V, int S, int prefetch, int32_t* __restrict__ acc_len,
+                   int32_t* __restrict__ acc_tokens, int32_t* __restrict__ acc_nodes,
+                   int32_t* __restrict__ bonus, int32_t* d_err) {
+  __shared__ int32_t par_s[kMaxB], tok_s[kMaxB];
+  __shared__ ArgPart part[2];                     // this CTA's partial, by level parity
+  __shared__ ArgPart warp_best[kPathThreads / 32];
+  __shared__ int a_s, child_s;
+  constexpr unsigned kFull = 0xFFFFFFFFu;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x / S, rank = blockIdx.x % S;
+  const int n = n_nodes[b];
+
+  // Validate and stage the tree (every CTA of the cluster reaches the same verdict).
+  int flag = (n < 0 || n > B) ? JT_DEVERR_NNODES : 0;
+  if (!flag) {
+    for (int v = tid; v < n; v += kPathThreads) {
+      const int pv = parent[(size_t)b * B + v], t = token[(size_t)b * B + v];
+      if (pv < -1 || pv >= v) flag |= JT_DEVERR_PARENT;
+      if (t < 0 || t >= V) flag |= JT_DEVERR_TOKEN;
+      par_s[v] = pv;
+      tok_s[v] = t;
+    }
+  }
+  const int bad = __syncthreads_or(flag);
+  int32_t* at = acc_tokens + (size_t)b * N;
+  int32_t* an = acc_nodes + (size_t)b * N;
+  if (bad) {  // uniform over the cluster: nobody touches DSMEM
+    if (rank == 0) {
+      if (flag) raise_flag(d_err, flag);
+      for (int i = tid; i < N; i += kPathThreads) { at[i] = -1; an[i] = -1; }
+      if (tid == 0) { acc_len[b] = 0; bonus[b] = -1; }
+    }
+    return;
+  }
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int v4 = V >> 2;
+  const int per = (v4 + S - 1) / S;
+  const int lo = min(v4, rank * per), hi = min(v4, lo + per);
+  const float* rows = target + (size_t)b * (B + 1) * V;
+  int cur = -1, row = 0, len = 0, a = -1;
+  for (int level = 0;; ++level) {
+    // Prefetch this CTA's segment of every child row (one of them is next).
+    if (prefetch && tid < n && par_s[tid] == cur && hi > lo)
+      prefetch_l2_bulk(rows + (size_t)(1 + tid) * V + 4 * lo, (uint32_t)(hi - lo) * 16u);
+    // Scan this CTA's segment of the current row: max, lowest index on ties.
+    const float4* r4 = reinterpret_cast<const float4*>(rows + (size_t)row * V);
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int j0 = lo + tid; j0 < hi; j0 += 4 * kPathThreads) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kPathThreads;
+        x[u] = j < hi ? ld_stream(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kPathThreads;
+        if (j < hi) {
+          if (x[u].x > bv || bi == INT_MAX) { bv = x[u].x; bi = 4 * j; }
+          if (x[u].y > bv) { bv = x[u].y; bi = 4 * j + 1; }
+          if (x[u].z > bv) { bv = x[u].z; bi = 4 * j + 2; }
+          if (x[u].w > bv) { bv = x[u].w; bi = 4 * j + 3; }
+        }
+      }
+    }
+    {
+      const uint32_t key = bi == INT_MAX ? 0u : order_key(bv);
+      const uint32_t top = __reduce_max_sync(kFull, key);
+      const uint32_t idx = __reduce_min_sync(kFull, (key == top && bi != INT_MAX) ? (uint32_t)bi : 0xFFFFFFFFu);
+      const float wvv = __shfl_sync(kFull, bv, __ffs(__ballot_sync(kFull, key == top && (uint32_t)bi == idx && bi != INT_MAX)) - 1);
+      if (lane == 0) warp_best[warp] = ArgPart{top == 0 ? -INFINITY : wvv, top == 0 ? INT_MAX : (int)idx};
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const ArgPart wp = lane < kPathThreads / 32 ? warp_best[lane] : ArgPart{-INFINITY, INT_MAX};
+      const uint32_t key = wp.i == INT_MAX ? 0u : order_key(wp.v);
+      const uint32_t top = __reduce_max_sync(kFull, key);
+      const uint32_t idx = __reduce_min_sync(kFull, (key == top && wp.i != INT_MAX) ? (uint32_t)wp.i : 0xFFFFFFFFu);
+      const float wvv = __shfl_sync(kFull, wp.v, __ffs(__ballot_sync(kFull, key == top && (uint32_t)wp.i == idx && wp.i != INT_MAX)) - 1);
+      if (lane == 0) part[level & 1] = ArgPart{top == 0 ? -INFINITY : wvv, top == 0 ? INT_MAX : (int)idx};
+    }
+    cluster.sync();  // every CTA's partial for this level is visible
+    if (warp == 0) {
+      ArgPart rp = {-INFINITY, INT_MAX};
+      if (lane < S) rp = cluster.map_shared_rank(part, lane)[level & 1];
+      const uint32_t key = rp.i == INT_MAX ? 0u : order_key(rp.v);
+      const uint32_t top = __reduce_max_sync(kFull, key);
+      const uint32_t idx = __reduce_min_sync(kFull, (key == top && rp.i != INT_MAX) ? (uint32_t)rp.i : 0xFFFFFFFFu);
+      if (lane == 0) { a_s = (int)idx; child_s = INT_MAX; }
+    }
+    __syncthreads();
+    a = a_s;
+    if (tid < n && par_s[tid] == cur && tok_s[tid] == a) atomicMin(&child_s, tid);
+    __syncthreads();
+    const int c = child_s;
+    if (c == INT_MAX || len >= N) break;   // uniform over the cluster
+    if (rank == 0 && tid == 0) { at[len] = a; an[len] = c; }
+    ++len;
+    cur = c;
+    row = 1 + c;
+    __syncthreads();   // child_s / a_s are rewritten next level
+  }
+  if (rank == 0) {
+    for (int i = len + tid; i < N; i += kPathThreads) { at[i] = -1; an[i] = -1; }
+    if (tid == 0) { acc_len[b] = len; bonus[b] = a; }
+  }
+  cluster.sync();  // keep this CTA's partials alive until every rank has read them
+}
+
+bool use_path_walk(int B, int n_depth) { return (B + 1) > 4 * (n_depth + 1); }
+
 }  // namespace
 
-size_t accept_workspace_bytes(int batch, int B, int vocab) {
+size_t accept_workspace_bytes(int batch, int B, int n_depth, int vocab) {
   (void)vocab;
+  if (use_path_walk(B, n_depth)) return 0;
   return align_up((size_t)batch * (B + 1) * sizeof(int32_t), 256);
 }
 
@@ -110,6 +246,30 @@ cudaError_t launch_tree_accept(const Ctx& c, const float* target, const int32_t*
                                int n_depth, int vocab, int32_t* acc_len, int32_t* acc_tokens,
                                int32_t* acc_nodes, int32_t* bonus) {
   if (batch == 0) return cudaSuccess;
+  if (use_path_walk(B, n_depth)) {
+    // Cluster size: enough CTAs for ~4 per SM, at most 16 per sequence.
+    int S = 1;
+    while (S < 16 && (long)batch * S * 2 <= 4L * c.num_sms && (vocab / 4) / (2 * S) >= 1024) S *= 2;
+    const int prefetch = (long)batch * B <= 64L * 64 ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(batch * S);
+    cfg.blockDim = dim3(kPathThreads);
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (S > 8) {
+      cudaError_t e = cudaFuncSetAttribute(accept_path_kernel,
+                                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaLaunchKernelEx(&cfg, accept_path_kernel, target, parent, token, n_nodes, B, n_depth,
+                              vocab, S, prefetch, acc_len, acc_tokens, acc_nodes, bonus, c.d_err);
+  }
   int32_t* am = static_cast<int32_t*>(c.workspace);
   const long rows = (long)batch * (B + 1);
   const int S = pick_row_split(rows, vocab / 4, c.num_sms, 16);

@@ -167,9 +167,9 @@ jt_status jt_tree_attn(const jt_attn_args* args, const jt_exec* exec) {
   return from_cuda(launch_tree_attn(c, *args));
 }
 
-size_t jt_tree_accept_workspace_bytes(int batch, int B, int vocab) {
-  if (batch < 0 || B < 1 || B > kMaxB || vocab < 1) return 0;
-  return accept_workspace_bytes(batch, B, vocab);
+size_t jt_tree_accept_workspace_bytes(int batch, int B, int n_depth, int vocab) {
+  if (batch < 0 || B < 1 || B > kMaxB || n_depth < 1 || n_depth > kMaxDepth || vocab < 1) return 0;
+  return accept_workspace_bytes(batch, B, n_depth, vocab);
 }
 
 jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, const int32_t* token,
@@ -189,7 +189,7 @@ jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, cons
   Ctx c;
   jt_status st = make_ctx(exec, &c);
   if (st != JT_OK) return st;
-  st = need_workspace(c, accept_workspace_bytes(batch, B, vocab));
+  st = need_workspace(c, accept_workspace_bytes(batch, B, n_depth, vocab));
   if (st != JT_OK) return st;
   return from_cuda(launch_tree_accept(c, target_logits, parent, token, n_nodes, batch, B, n_depth,
                                       vocab, acc_len, acc_tokens, acc_nodes, bonus));

@@ -34,6 +34,7 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
                    int N, int W, int B, int32_t* __restrict__ parent_o,
                    int32_t* __restrict__ token_o, int32_t* __restrict__ depth_o,
                    float* __restrict__ score_o, int32_t* __restrict__ n_nodes_o) {
+  __shared__ float score_s[kWarpsPerBlock][kMaxB];
   __shared__ uint8_t depth_s[kWarpsPerBlock][kMaxB];
   extern __shared__ int32_t cand_s[];   // per warp: N*W tokens then N*W log-probs
   const int warp = threadIdx.x >> 5;
@@ -54,12 +55,16 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
   int32_t* tko = token_o + (size_t)b * B;
   int32_t* dpo = depth_o + (size_t)b * B;
   float* sco = score_o + (size_t)b * B;
+  float* scs = score_s[warp];
   uint8_t* dep = depth_s[warp];
 
-  float fs[SLOTS];
+  // Frontier keys of this lane's slots (node (slot << 5) | lane); 0 = empty.
+  // best_key / best_slot cache the lane's own best (highest key, lowest slot).
+  uint32_t fk[SLOTS];
 #pragma unroll
-  for (int k = 0; k < SLOTS; ++k) fs[k] = 0.0f;
-  uint32_t alive = 0;  // bit k: slot k holds a frontier node
+  for (int k = 0; k < SLOTS; ++k) fk[k] = 0u;
+  uint32_t best_key = 0u;
+  int best_slot = 0;
 
   int count = 0;
   int cur = -1;          // the node being expanded; the root first
@@ -77,6 +82,7 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
       tko[v] = t;
       dpo[v] = d;
       sco[v] = csc;
+      scs[v] = csc;
       dep[v] = (uint8_t)d;
     }
     // Owner lane of child v = count + r is lane v & 31, i.e. r = (lane - count) & 31.
@@ -84,34 +90,37 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
     const float sv = __shfl_sync(kFull, csc, r);
     if (d < N && r < nc) {
       const int slot = (count + r) >> 5;
+      const uint32_t key = order_key(sv);
 #pragma unroll
       for (int k = 0; k < SLOTS; ++k)
-        if (k == slot) fs[k] = sv;
-      alive |= 1u << slot;
+        if (k == slot) fk[k] = key;
+      // A new node has a higher id than every node of its lane, so it
+      // displaces the cached best only with a strictly higher key.
+      if (key > best_key) { best_key = key; best_slot = slot; }
     }
     count += nc;
     __syncwarp();
     if (count >= B) break;
 
     // Pop: best (key desc, id asc) over the frontier.
-    uint32_t key = 0;   // 0 = empty (every float maps above 0)
-    int slot_best = 0;
-    float val_best = 0.0f;
-#pragma unroll
-    for (int k = 0; k < SLOTS; ++k) {
-      if ((alive >> k) & 1u) {
-        const uint32_t kk = order_key(fs[k]);
-        if (kk > key) { key = kk; slot_best = k; val_best = fs[k]; }
-      }
-    }
-    const uint32_t top = __reduce_max_sync(kFull, key);
+    const uint32_t top = __reduce_max_sync(kFull, best_key);
     if (top == 0) break;  // nothing expandable
-    const uint32_t my_id = (key == top) ? (uint32_t)((slot_best << 5) | lane) : 0xFFFFFFFFu;
-    const uint32_t id = __reduce_min_sync(kFull, my_id);
-    const int owner = (int)(id & 31u);
-    cur_s = __shfl_sync(kFull, val_best, owner);
-    if (lane == owner) alive &= ~(1u << (id >> 5));
+    const uint32_t id = __reduce_min_sync(
+        kFull, best_key == top ? (uint32_t)((best_slot << 5) | lane) : 0xFFFFFFFFu);
+    if ((int)(id & 31u) == lane) {
+      // The owner drops the popped slot and rescans its remaining slots.
+      const int ps = (int)(id >> 5);
+#pragma unroll
+      for (int k = 0; k < SLOTS; ++k)
+        if (k == ps) fk[k] = 0u;
+      best_key = 0u;
+      best_slot = 0;
+#pragma unroll
+      for (int k = SLOTS - 1; k >= 0; --k)
+        if (fk[k] >= best_key && fk[k] != 0u) { best_key = fk[k]; best_slot = k; }
+    }
     cur = (int)id;
+    cur_s = scs[cur];
     cur_d = dep[cur];
   }
   for (int v = count + lane; v < B; v += 32) {

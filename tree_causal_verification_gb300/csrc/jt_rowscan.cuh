@@ -1,17 +1,20 @@
 // Full-vocabulary row scans: top-K (value desc, index asc) and the
 // log-sum-exp of a row of fp32 logits, streamed once from HBM.
 //
-// Layout of the work: a row of V floats is cut into S segments (S = the
-// cluster size, 1..16). The S CTAs of a thread-block cluster each stream one
-// segment with 128-bit non-allocating loads, UNROLL float4s per thread in
-// flight, keeping per thread a sorted top-K list in registers and an online
-// (max, sum exp) pair. Lists are merged warp-wide with xor shuffles (a
-// bitonic half-cleaner keeps the better half of two sorted lists, then
-// log2 K compare-exchange stages re-sort it), then across warps through
-// shared memory, then across the cluster: after a cluster barrier, CTA rank
-// 0 reads the other CTAs' partials straight out of their shared memory
-// (distributed shared memory) and finishes the row. No global scratch, no
-// atomics, no second launch.
+// Work layout: a row of V floats is cut into S segments (S = the cluster
+// size, 1..16); each CTA of a thread-block cluster streams one segment with
+// 128-bit non-allocating loads, two batches of float4s per thread in flight.
+// Per thread: a sorted top-K list in registers, guarded by a one-compare
+// rejection test of each float4's maximum against the current K-th value,
+// and an online log-sum-exp in the log2 domain.
+//
+// Selection (warp, then block, then cluster) runs K rounds of a warp-wide
+// argmax: every lane offers its best remaining candidate; __reduce_max_sync
+// over an order-preserving uint32 key of the value picks the winning value,
+// __reduce_min_sync over the indices holding it breaks ties towards the
+// lower token id, and the winning lane advances to its next candidate.
+// The cluster's CTAs hand their partials to CTA rank 0 through distributed
+// shared memory. No global scratch, no atomics, no second launch.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -24,20 +27,32 @@ namespace cg = cooperative_groups;
 
 constexpr int kScanThreads = 256;
 constexpr int kScanWarps = kScanThreads / 32;
-constexpr int kScanUnroll = 8;
+constexpr int kScanBatch = 4;     // float4s per thread per batch (two batches in flight)
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <int K>
 struct TopK {
   float v[K];
   int i[K];
+  int n;   // real elements inserted so far (the first K always enter)
 
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int k = 0; k < K; ++k) { v[k] = -INFINITY; i[k] = INT_MAX; }
+    n = 0;
   }
 
+  // Elements must arrive in increasing index order within a thread, so a
+  // later element that ties the K-th value never displaces it.
   __device__ __forceinline__ void push(float x, int idx) {
-    if (!ranks_before(x, idx, v[K - 1], i[K - 1])) return;
+    if (n >= K && !(x > v[K - 1])) return;
+    ++n;
     v[K - 1] = x;
     i[K - 1] = idx;
 #pragma unroll
@@ -49,53 +64,19 @@ struct TopK {
     }
   }
 
-  // Keep the best K of (this ∪ other); both sorted, result sorted.
-  __device__ __forceinline__ void merge(const float (&ov)[K], const int (&oi)[K]) {
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      if (ranks_before(ov[K - 1 - k], oi[K - 1 - k], v[k], i[k])) {
-        v[k] = ov[K - 1 - k];
-        i[k] = oi[K - 1 - k];
-      }
-    }
-    // v is now bitonic; sort descending with half-cleaners.
-#pragma unroll
-    for (int j = K / 2; j > 0; j >>= 1) {
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const int p = k ^ j;
-        if (p > k && ranks_before(v[p], i[p], v[k], i[k])) {
-          const float tv = v[k]; v[k] = v[p]; v[p] = tv;
-          const int ti = i[k]; i[k] = i[p]; i[p] = ti;
-        }
-      }
-    }
-  }
-
-  __device__ __forceinline__ void warp_merge(unsigned mask = 0xFFFFFFFFu) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float ov[K];
-      int oi[K];
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        ov[k] = __shfl_xor_sync(mask, v[k], off);
-        oi[k] = __shfl_xor_sync(mask, i[k], off);
-      }
-      merge(ov, oi);
-    }
-  }
+  __device__ __forceinline__ float threshold() const { return n >= K ? v[K - 1] : -INFINITY; }
 };
 
-// Online log-sum-exp: the row's running max m and s = sum exp(x - m).
+// Online log-sum-exp in log2 units: the row's running max m (of x*log2e)
+// and s = sum 2^(x*log2e - m).
 struct Lse {
   float m, s;
   __device__ __forceinline__ void init() { m = -INFINITY; s = 0.0f; }
   __device__ __forceinline__ void combine(float m2, float s2) {
     if (m2 == -INFINITY) return;
     if (m == -INFINITY) { m = m2; s = s2; return; }
-    if (m2 > m) { s = s * __expf(m - m2) + s2; m = m2; }
-    else { s = s + s2 * __expf(m2 - m); }
+    if (m2 > m) { s = s * fast_ex2(m - m2) + s2; m = m2; }
+    else { s = s + s2 * fast_ex2(m2 - m); }
   }
   __device__ __forceinline__ void warp_reduce() {
 #pragma unroll
@@ -115,7 +96,7 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) {
   return r;
 }
 
-// Per-CTA partial result kept in shared memory for the cluster merge.
+// A candidate list handed between selection levels.
 template <int K>
 struct ScanPartial {
   float v[K];
@@ -123,81 +104,137 @@ struct ScanPartial {
   float m, s;
 };
 
-// Streams floats [lo4*4, hi4*4) of `row` into per-thread state.
+// K rounds of warp-wide argmax. Lane l offers the sorted list (cv, ci) of
+// length `len`; on return every lane holds the warp's best K in out_v/out_i.
+template <int K, int L>
+__device__ __forceinline__ void warp_select(const float (&cv)[L], const int (&ci)[L], int len,
+                                            float (&out_v)[K], int (&out_i)[K]) {
+  constexpr unsigned kFull = 0xFFFFFFFFu;
+  const int lane = threadIdx.x & 31;
+  int head = 0;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    float hv = -INFINITY;
+    int hi = INT_MAX;
+#pragma unroll
+    for (int q = 0; q < L; ++q)
+      if (q == head && q < len) { hv = cv[q]; hi = ci[q]; }
+    const bool live = head < len;
+    // key 0 = nothing left in this lane; every real value maps above 0.
+    const uint32_t key = live ? order_key(hv) : 0u;
+    const uint32_t top = __reduce_max_sync(kFull, key);
+    const uint32_t idx = __reduce_min_sync(kFull, (live && key == top) ? (uint32_t)hi : 0xFFFFFFFFu);
+    // The winner: the lane whose head has that key and index.
+    const bool win = live && key == top && (uint32_t)hi == idx;
+    const float wv = __shfl_sync(kFull, hv, __ffs(__ballot_sync(kFull, win)) - 1);
+    out_v[k] = top == 0 ? -INFINITY : wv;
+    out_i[k] = top == 0 ? INT_MAX : (int)idx;
+    if (win) ++head;
+    (void)lane;
+  }
+}
+
+// Streams float4s [lo4, hi4) of `row` into per-thread state.
 template <int K, bool LSE>
 __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int lo4, int hi4,
                                              TopK<K>& top, Lse& lse) {
   const float4* r4 = reinterpret_cast<const float4*>(row);
-  for (int base = lo4 + (int)threadIdx.x; base < hi4; base += kScanThreads * kScanUnroll) {
-    float4 x[kScanUnroll];
+  constexpr int STEP = kScanThreads * kScanBatch;
+  float4 cur[kScanBatch], nxt[kScanBatch];
+  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  int base = lo4 + (int)threadIdx.x;
 #pragma unroll
-    for (int u = 0; u < kScanUnroll; ++u) {
-      const int j = base + u * kScanThreads;
-      x[u] = (j < hi4) ? ld_stream(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  for (int u = 0; u < kScanBatch; ++u) {
+    const int j = base + u * kScanThreads;
+    cur[u] = (j < hi4) ? ld_stream(r4 + j) : ninf;
+  }
+  for (; base < hi4; base += STEP) {
+    // Next batch in flight while this one is processed.
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) {
+      const int j = base + STEP + u * kScanThreads;
+      nxt[u] = (j < hi4) ? ld_stream(r4 + j) : ninf;
     }
     if (LSE) {
       float bm = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kScanUnroll; ++u)
-        bm = fmaxf(bm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
-      if (bm > lse.m) {
-        lse.s = (lse.m == -INFINITY) ? 0.0f : lse.s * __expf(lse.m - bm);
-        lse.m = bm;
+      for (int u = 0; u < kScanBatch; ++u)
+        bm = fmaxf(bm, fmaxf(fmaxf(cur[u].x, cur[u].y), fmaxf(cur[u].z, cur[u].w)));
+      const float bm2 = bm * kLog2e;
+      if (bm2 > lse.m) {
+        lse.s = (lse.m == -INFINITY) ? 0.0f : lse.s * fast_ex2(lse.m - bm2);
+        lse.m = bm2;
       }
       if (lse.m != -INFINITY) {
         float acc = 0.0f;
 #pragma unroll
-        for (int u = 0; u < kScanUnroll; ++u)
-          acc += __expf(x[u].x - lse.m) + __expf(x[u].y - lse.m) + __expf(x[u].z - lse.m) +
-                 __expf(x[u].w - lse.m);
+        for (int u = 0; u < kScanBatch; ++u)
+          acc += fast_ex2(fmaf(cur[u].x, kLog2e, -lse.m)) + fast_ex2(fmaf(cur[u].y, kLog2e, -lse.m)) +
+                 fast_ex2(fmaf(cur[u].z, kLog2e, -lse.m)) + fast_ex2(fmaf(cur[u].w, kLog2e, -lse.m));
         lse.s += acc;
       }
     }
 #pragma unroll
-    for (int u = 0; u < kScanUnroll; ++u) {
+    for (int u = 0; u < kScanBatch; ++u) {
       const int j = base + u * kScanThreads;
-      if (j < hi4) {
-        top.push(x[u].x, 4 * j);
-        top.push(x[u].y, 4 * j + 1);
-        top.push(x[u].z, 4 * j + 2);
-        top.push(x[u].w, 4 * j + 3);
+      const float4 x = cur[u];
+      const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+      if (j < hi4 && (top.n < K || mx > top.threshold())) {
+        top.push(x.x, 4 * j);
+        top.push(x.y, 4 * j + 1);
+        top.push(x.z, 4 * j + 2);
+        top.push(x.w, 4 * j + 3);
       }
+      cur[u] = nxt[u];
     }
   }
 }
 
-// Reduces the CTA's per-thread state into `out` (valid in thread 0's view of
-// shared memory after the trailing __syncthreads).
+// Reduces the CTA's per-thread state into `out` (valid after the trailing
+// __syncthreads).
 template <int K, bool LSE>
 __device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial<K>* out,
                                              ScanPartial<K>* warp_parts) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  top.warp_merge();
+  float wv[K];
+  int wi[K];
+  warp_select<K, K>(top.v, top.i, min(top.n, K), wv, wi);
   if (LSE) lse.warp_reduce();
   if (lane == 0) {
 #pragma unroll
-    for (int k = 0; k < K; ++k) { warp_parts[warp].v[k] = top.v[k]; warp_parts[warp].i[k] = top.i[k]; }
+    for (int k = 0; k < K; ++k) { warp_parts[warp].v[k] = wv[k]; warp_parts[warp].i[k] = wi[k]; }
     warp_parts[warp].m = lse.m;
     warp_parts[warp].s = lse.s;
   }
   __syncthreads();
   if (warp == 0) {
-    TopK<K> t;
+    // kScanWarps lists of K: lane l takes list l (the lists are sorted).
+    float cv[K];
+    int ci[K];
     Lse l;
+    int len = 0;
     if (lane < kScanWarps) {
 #pragma unroll
-      for (int k = 0; k < K; ++k) { t.v[k] = warp_parts[lane].v[k]; t.i[k] = warp_parts[lane].i[k]; }
+      for (int k = 0; k < K; ++k) { cv[k] = warp_parts[lane].v[k]; ci[k] = warp_parts[lane].i[k]; }
+      len = K;
       l.m = warp_parts[lane].m;
       l.s = warp_parts[lane].s;
     } else {
-      t.init();
+#pragma unroll
+      for (int k = 0; k < K; ++k) { cv[k] = -INFINITY; ci[k] = INT_MAX; }
       l.init();
     }
-    t.warp_merge();
+    // Short lists (fewer than K real elements) end in sentinels: count the rest.
+    len = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) len += (ci[k] != INT_MAX);
+    float bv[K];
+    int bi[K];
+    warp_select<K, K>(cv, ci, len, bv, bi);
     if (LSE) l.warp_reduce();
     if (lane == 0) {
 #pragma unroll
-      for (int k = 0; k < K; ++k) { out->v[k] = t.v[k]; out->i[k] = t.i[k]; }
+      for (int k = 0; k < K; ++k) { out->v[k] = bv[k]; out->i[k] = bi[k]; }
       out->m = l.m;
       out->s = l.s;
     }
@@ -205,8 +242,9 @@ __device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial
   __syncthreads();
 }
 
-// Merge the cluster's partials in CTA rank 0 (warp 0). Returns true in the
-// thread that holds the final result (lane 0 of warp 0 of rank 0).
+// Merges the cluster's partials in CTA rank 0 (warp 0). Returns true in the
+// thread that holds the final result (lane 0 of warp 0 of rank 0), with the
+// list in top.v/top.i and the log-sum-exp state in lse.
 template <int K, bool LSE>
 __device__ __forceinline__ bool cluster_reduce(ScanPartial<K>* mine, int S, TopK<K>& top,
                                                Lse& lse) {
@@ -223,17 +261,25 @@ __device__ __forceinline__ bool cluster_reduce(ScanPartial<K>* mine, int S, TopK
   bool holder = false;
   if (cluster.block_rank() == 0 && threadIdx.x < 32) {
     const int lane = threadIdx.x;
+    float cv[K];
+    int ci[K];
+    int len = 0;
     if (lane < S) {
       const ScanPartial<K>* p = cluster.map_shared_rank(mine, lane);
 #pragma unroll
-      for (int k = 0; k < K; ++k) { top.v[k] = p->v[k]; top.i[k] = p->i[k]; }
+      for (int k = 0; k < K; ++k) { cv[k] = p->v[k]; ci[k] = p->i[k]; }
+      len = K;
       lse.m = p->m;
       lse.s = p->s;
     } else {
-      top.init();
+#pragma unroll
+      for (int k = 0; k < K; ++k) { cv[k] = -INFINITY; ci[k] = INT_MAX; }
       lse.init();
     }
-    top.warp_merge();
+    len = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) len += (ci[k] != INT_MAX);
+    warp_select<K, K>(cv, ci, len, top.v, top.i);
     if (LSE) lse.warp_reduce();
     holder = (lane == 0);
   }
@@ -242,7 +288,7 @@ __device__ __forceinline__ bool cluster_reduce(ScanPartial<K>* mine, int S, TopK
 }
 
 // Picks the cluster size (segments per row) for `rows` rows of `v4` float4s:
-// enough CTAs to cover the SMs a few times, segments of >= 2048 float4s.
+// enough CTAs to cover the SMs twice, segments of >= 2048 float4s.
 inline int pick_row_split(long rows, int v4, int num_sms, int max_split) {
   int s = 1;
   while (s < max_split && rows * s < 2L * num_sms && (v4 / (2 * s)) >= 2048) s *= 2;

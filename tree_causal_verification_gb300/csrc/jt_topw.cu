@@ -34,12 +34,14 @@ topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __re
   scan_segment<K, true>(logits + (size_t)row * V, lo, hi, top, lse);
   block_reduce<K, true>(top, lse, &part, warp_parts);
   if (cluster_reduce<K, true>(&part, S, top, lse)) {
-    const float logZ = logf(lse.s);
+    // lse.m is the max of x*log2(e) and lse.s = sum 2^(x*log2(e) - m), so
+    // ln Z = m * ln 2 + ln s.
+    const float lnZ = fmaf(lse.m, 0.6931471805599453f, logf(lse.s));
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       if (k < W) {
         tok[(size_t)row * W + k] = top.i[k];
-        logp[(size_t)row * W + k] = (top.v[k] - lse.m) - logZ;
+        logp[(size_t)row * W + k] = top.v[k] - lnZ;
       }
     }
   }

@@ -86,7 +86,7 @@ def load(path: str = LIB_PATH):
             lib.jt_tree_attn_workspace_bytes.argtypes = [ctypes.POINTER(jt_attn_args)]
             lib.jt_tree_attn.argtypes = [ctypes.POINTER(jt_attn_args), _pexec]
             lib.jt_tree_accept_workspace_bytes.restype = _c_size
-            lib.jt_tree_accept_workspace_bytes.argtypes = [_c_int] * 3
+            lib.jt_tree_accept_workspace_bytes.argtypes = [_c_int] * 4
             lib.jt_tree_accept.argtypes = [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                            _vp, _vp, _vp, _vp, _pexec]
             lib.jt_tree_accept_noalloc.argtypes = lib.jt_tree_accept.argtypes
@@ -285,7 +285,7 @@ def jt_tree_accept(target, parent, token, n_nodes, n_depth, out=None, exec=None)
     _need(token, torch.int32, (batch, B), "token")
     _need(n_nodes, torch.int32, (batch,), "n_nodes")
     lib = load()
-    ex = _exec(exec).reserve(lib.jt_tree_accept_workspace_bytes(batch, B, V))
+    ex = _exec(exec).reserve(lib.jt_tree_accept_workspace_bytes(batch, B, n_depth, V))
     c = ex.c()
     _check(lib.jt_tree_accept(_ptr(target), _ptr(parent), _ptr(token), _ptr(n_nodes), batch, B,
                               n_depth, V, _ptr(out["acc_len"]), _ptr(out["acc_tokens"]),
