@@ -18,20 +18,27 @@
 //
 // One CTA per unit (or per slice of its key tiles when units are too few to
 // fill the GPU: split-KV over a thread-block cluster, merged in distributed
-// shared memory). 320 threads:
+// shared memory). 384 threads = 3 warpgroups; setmaxnreg moves registers
+// from the third (producer / MMA, 88 each) to the two softmax warpgroups
+// (208 each) for the main loop; 384 x 168 = 256 x 208 + 128 x 88:
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread r of a
-//              warpgroup owns TMEM lane r (= query row). Pass 1 reads S from
-//              TMEM and finds the row max (prefix bound / ancestor bits /
-//              scale applied in registers); pass 2 re-reads S, forms
+//              warpgroup owns TMEM lane r (= query row). It loads the row's
+//              128 scores of S from TMEM once, applies the prefix bound /
+//              ancestor bits / scale in registers, takes the row max, forms
 //              P = 2^(s - m) and writes it back over S in TMEM as packed bf16.
 //              O is rescaled in TMEM only when a row max grows by more than
 //              2^8 (lazy rescaling; the final 1/l uses the same stale max);
-//   warp 8     TMA producer: Q_A, Q_B once, then K and V into a 2-stage ring;
+//   warp 8     TMA producer of Q_A, Q_B (once) and of K tiles into a 2-slot ring;
+//   warp 10    TMA producer of V tiles into a second 2-slot ring. A K slot is
+//              released as soon as both tiles' S MMAs have read it, a V slot
+//              after both P V MMAs, so K tile j+2 streams in while tile j+1
+//              is still being processed;
+//   warp 11    idle (completes the third warpgroup);
 //   warp 9     TMEM owner and MMA issuer (one thread), per K/V tile j:
 //              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), where
 //              S_X = Q_X K^T (M=128, N=128, K=D, operands in shared memory)
-//              O_X += P_X V  (M=128, N=64 per half of D, K=128 keys; P from
-//                             TMEM, V from shared memory, MN-major)
+//              O_X += P_X V  (M=128, N=D, K=128 keys; P from TMEM, V from
+//                             shared memory, MN-major)
 //              so one tile's softmax overlaps the other tile's MMAs. Tensor
 //              ops retire in issue order, so the commit after S_X(j+1) also
 //              certifies that PV_X(j) has finished with P_X / O_X.
@@ -53,8 +60,9 @@ namespace {
 namespace cg = cooperative_groups;
 using namespace sm100;
 
-constexpr int kThreads = 320;
-constexpr int kWarpTMA = 8, kWarpMMA = 9;
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsSoftmax = 208, kRegsOther = 88, kRegsLaunch = 168;
+constexpr int kWarpTMA = 8, kWarpMMA = 9, kWarpTMAV = 10;
 constexpr int kTile = 128;                 // query rows per M tile = keys per K/V tile
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
@@ -74,7 +82,8 @@ struct AttnParams {
 };
 
 struct Bars {
-  uint64_t q_full, kv_full[kStages], kv_empty[kStages], s_full[2], p_full[2], pv_done[2], drain;
+  uint64_t q_full, k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_full[2], pv_done[2], drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -158,8 +167,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -192,30 +203,52 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     return t < p_tiles ? min(kTile, L - t * kTile) : min(kTile, n - (t - p_tiles) * kTile);
   };
 
-  if (warp == kWarpTMA) {
-    // =================== TMA producer ===================
+  // Softmax state, read by the common epilogue.
+  float m_run = -INFINITY, l_run = 0.0f;
+  const int X = warp >> 2;
+  const int r = tid & 127;
+  const int R = X * kTile + r;              // row within the unit's 256
+  const int v = v0 + R / g;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t s_col = tmem + lane_base + X * 128;
+  const uint32_t o_col = tmem + lane_base + 256 + X * OSTRIDE;
+  const bool tile_live = X == 0 || twoB;
+  bool sm_ok = true;
+
+  if (warp >= 8) {
+  // Third warpgroup: producer, MMA issuer, two idle warps. Lean registers.
+  regs_dec<kRegsOther>();
+  if (warp == kWarpTMA || warp == kWarpTMAV) {
+    // =================== TMA producers (warp 8: Q and K, warp 10: V) ===================
+    const bool is_v = warp == kWarpTMAV;
     if (lane == 0 && T > 0) {
-      tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mkc);
-      tma_prefetch_desc(&mvc);
-      tma_prefetch_desc(&mkt);
-      tma_prefetch_desc(&mvt);
-      mbar_arrive_expect_tx(&bars->q_full, (twoB ? 2 : 1) * QB);
-      for (int X = 0; X < (twoB ? 2 : 1); ++X)
+      if (!is_v) {
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mkc);
+        tma_prefetch_desc(&mkt);
+        mbar_arrive_expect_tx(&bars->q_full, (twoB ? 2 : 1) * QB);
+        for (int X2 = 0; X2 < (twoB ? 2 : 1); ++X2)
 #pragma unroll
-        for (int ch = 0; ch < CH; ++ch)
-          tma_load_4d(sQ(X) + ch * CHB, &mq, &bars->q_full, ch * 64, kh * g, v0 + X * npt, b);
+          for (int ch = 0; ch < CH; ++ch)
+            tma_load_4d(sQ(X2) + ch * CHB, &mq, &bars->q_full, ch * 64, kh * g, v0 + X2 * npt, b);
+      } else {
+        tma_prefetch_desc(&mvc);
+        tma_prefetch_desc(&mvt);
+      }
+      const CUtensorMap* mc = is_v ? &mvc : &mkc;
+      const CUtensorMap* mtr = is_v ? &mvt : &mkt;
+      uint64_t* full = is_v ? bars->v_full : bars->k_full;
+      uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
       const int np = (L + kPageSize - 1) / kPageSize;
       for (int jt = 0; jt < T; ++jt) {
         const int t = t_begin + jt, st = jt % kStages;
         if (jt >= kStages &&
-            !mbar_wait(&bars->kv_empty[st], ((jt / kStages) + 1) & 1, abort, kWaitBudget)) {
+            !mbar_wait(&empty[st], ((jt / kStages) + 1) & 1, abort, kWaitBudget)) {
           fail();
           break;
         }
-        mbar_arrive_expect_tx(&bars->kv_full[st], 2 * QB);
-        uint8_t* dk = sK(st);
-        uint8_t* dv = sV(st);
+        mbar_arrive_expect_tx(&full[st], QB);
+        uint8_t* dst = is_v ? sV(st) : sK(st);
         if (t < p_tiles) {
           const int key0 = t * kTile;
           if (p.paged) {
@@ -224,53 +257,48 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
               const int pi = key0 / kPageSize + pg;
               const int page = pi < np ? p.block_table[(size_t)b * p.max_pages + pi] : 0;
 #pragma unroll
-              for (int ch = 0; ch < CH; ++ch) {
-                tma_load_4d(dk + ch * CHB + pg * (kPageSize * 128), &mkc, &bars->kv_full[st],
-                            ch * 64, kh, 0, page);
-                tma_load_4d(dv + ch * CHB + pg * (kPageSize * 128), &mvc, &bars->kv_full[st],
-                            ch * 64, kh, 0, page);
-              }
+              for (int ch = 0; ch < CH; ++ch)
+                tma_load_4d(dst + ch * CHB + pg * (kPageSize * 128), mc, &full[st], ch * 64, kh, 0,
+                            page);
             }
           } else {
 #pragma unroll
-            for (int ch = 0; ch < CH; ++ch) {
-              tma_load_4d(dk + ch * CHB, &mkc, &bars->kv_full[st], ch * 64, kh, key0, b);
-              tma_load_4d(dv + ch * CHB, &mvc, &bars->kv_full[st], ch * 64, kh, key0, b);
-            }
+            for (int ch = 0; ch < CH; ++ch)
+              tma_load_4d(dst + ch * CHB, mc, &full[st], ch * 64, kh, key0, b);
           }
         } else {
           const int u0 = (t - p_tiles) * kTile;
 #pragma unroll
-          for (int ch = 0; ch < CH; ++ch) {
-            tma_load_4d(dk + ch * CHB, &mkt, &bars->kv_full[st], ch * 64, kh, u0, b);
-            tma_load_4d(dv + ch * CHB, &mvt, &bars->kv_full[st], ch * 64, kh, u0, b);
-          }
+          for (int ch = 0; ch < CH; ++ch)
+            tma_load_4d(dst + ch * CHB, mtr, &full[st], ch * 64, kh, u0, b);
         }
       }
     }
   } else if (warp == kWarpMMA) {
     // =================== MMA issuer ===================
     constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
-    constexpr uint32_t id_o = idesc_bf16(128, 64, 0, 1);
+    constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);   // N = D: one MMA per K step
+    // Descriptor bases (start address in the low 14 bits); each K step adds
+    // a constant byte offset >> 4, so no descriptor is rebuilt in the loop.
+    const uint64_t qd[2] = {sdesc_sw128(smem_u32(sQ(0)), 16, 1024), sdesc_sw128(smem_u32(sQ(1)), 16, 1024)};
+    const uint64_t kd[2] = {sdesc_sw128(smem_u32(sK(0)), 16, 1024), sdesc_sw128(smem_u32(sK(1)), 16, 1024)};
+    const uint64_t vd[2] = {sdesc_sw128(smem_u32(sV(0)), CHB, 1024), sdesc_sw128(smem_u32(sV(1)), CHB, 1024)};
     auto issue_s = [&](int X, int st) {
-      const uint32_t q_addr = smem_u32(sQ(X)), k_addr = smem_u32(sK(st));
+      const uint64_t q = qd[X], k = kd[st];
+      const uint32_t d = tmem + X * 128;
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
-        const uint32_t off = (kk >> 2) * CHB + (kk & 3) * 32;
-        mma_bf16_ss(tmem + X * 128, sdesc_sw128(q_addr + off, 16, 1024),
-                    sdesc_sw128(k_addr + off, 16, 1024), id_s, kk > 0);
+        const uint64_t off = (uint64_t)(((kk >> 2) * CHB + (kk & 3) * 32) >> 4);
+        mma_bf16_ss(d, q + off, k + off, id_s, kk > 0);
       }
       mma_commit(&bars->s_full[X]);
     };
     auto issue_pv = [&](int X, int jt) {
-      const uint32_t v_addr = smem_u32(sV(jt % kStages));
+      const uint64_t v = vd[jt % kStages];
+      const uint32_t d = tmem + 256 + X * OSTRIDE, a = tmem + X * 128;
 #pragma unroll
-      for (int h = 0; h < CH; ++h)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + 256 + X * OSTRIDE + 64 * h, tmem + X * 128 + kk * 8,
-                      sdesc_sw128(v_addr + h * CHB + kk * 2048, CHB, 1024), id_o,
-                      jt > 0 || kk > 0);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16_ts(d, a + kk * 8, v + (uint64_t)(kk * (2048 >> 4)), id_o, jt > 0 || kk > 0);
       mma_commit(&bars->pv_done[X]);
     };
     // Rows of V past a tile's valid keys may hold anything (NaN included); P
@@ -288,30 +316,34 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         __syncwarp();
       }
     };
-    bool ok = T > 0 && warp_wait(&bars->q_full, 0) && warp_wait(&bars->kv_full[0], 0);
+    bool ok = T > 0 && warp_wait(&bars->q_full, 0) && warp_wait(&bars->k_full[0], 0);
     if (T > 0 && !ok) fail();
     if (ok) {
-      zero_v_tail(0);
       tc_fence_after();
       if (lane == 0) {
         issue_s(0, 0);
         if (twoB) issue_s(1, 0);
+        mma_commit(&bars->k_empty[0]);   // K tile 0 is no longer needed
       }
       __syncwarp();
     }
     for (int jt = 0; ok && jt < T; ++jt) {
       const int st = jt % kStages;
       if (!warp_wait(&bars->p_full[0], jt & 1)) { fail(); ok = false; break; }
+      if (!warp_wait(&bars->v_full[st], (jt / kStages) & 1)) { fail(); ok = false; break; }
+      zero_v_tail(jt);
       tc_fence_after();
       if (lane == 0) issue_pv(0, jt);
       __syncwarp();
       const bool more = jt + 1 < T;
+      const int st1 = (jt + 1) % kStages;
       if (more) {
-        const int st1 = (jt + 1) % kStages;
-        if (!warp_wait(&bars->kv_full[st1], ((jt + 1) / kStages) & 1)) { fail(); ok = false; break; }
-        zero_v_tail(jt + 1);
+        if (!warp_wait(&bars->k_full[st1], ((jt + 1) / kStages) & 1)) { fail(); ok = false; break; }
         tc_fence_after();
-        if (lane == 0) issue_s(0, st1);
+        if (lane == 0) {
+          issue_s(0, st1);
+          if (!twoB) mma_commit(&bars->k_empty[st1]);
+        }
         __syncwarp();
       }
       if (twoB) {
@@ -321,25 +353,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         __syncwarp();
       }
       if (lane == 0) {
-        mma_commit(&bars->kv_empty[st]);
-        if (twoB && more) issue_s(1, (jt + 1) % kStages);
+        mma_commit(&bars->v_empty[st]);
+        if (twoB && more) {
+          issue_s(1, st1);
+          mma_commit(&bars->k_empty[st1]);
+        }
       }
       __syncwarp();
     }
   }
-
+  } else {
   // =================== softmax (warps 0-7, tile X = warp / 4) ===================
-  float m_run = -INFINITY, l_run = 0.0f;
-  const int X = warp >> 2;
-  const int r = tid & 127;
-  const int R = X * kTile + r;              // row within the unit's 256
-  const int v = v0 + R / g;
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t s_col = tmem + lane_base + X * 128;
-  const uint32_t o_col = tmem + lane_base + 256 + X * OSTRIDE;
-  const bool tile_live = X == 0 || twoB;
-  bool sm_ok = true;
-  if (warp < 8 && tile_live) {
+  regs_inc<kRegsSoftmax>();
+  if (tile_live) {
     const bool row_valid = v < n;
     uint32_t mrow[kMaxWords];
 #pragma unroll
@@ -363,31 +389,41 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         const uint32_t w01 = (c & 1) ? ws1 : ws0, w23 = (c & 1) ? ws3 : ws2;
         return (c & 2) ? w23 : w01;
       };
-      // Pass 1: row max of the visible scores. A prefix tile whose 128 keys
-      // are all visible needs no per-key test (the common case by far).
+      // All 128 scores of the row at once (one wait), then mask / scale / max.
+      // A prefix tile whose 128 keys are all visible needs no per-key test.
       const bool full = !tree && lim >= kTile;
-      float tmax = -INFINITY;
-      if (full) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tmem_ld32(s_col + c * 32, x);
-          tmem_wait_ld();
+      float x[kTile];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
+      for (int c = 0; c < 4; ++c) {
+        float tmp[32];
+        tmem_ld32(s_col + c * 32, tmp);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[c * 32 + i] = tmp[i];
+      }
+      tmem_wait_ld();
+      float tmax;
+      if (full) {
+        float m4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+        for (int i = 4; i < kTile; i += 4) {
+          m4[0] = fmaxf(m4[0], x[i]);
+          m4[1] = fmaxf(m4[1], x[i + 1]);
+          m4[2] = fmaxf(m4[2], x[i + 2]);
+          m4[3] = fmaxf(m4[3], x[i + 3]);
         }
-        tmax *= sl2;   // sl2 > 0
+        tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;   // sl2 > 0
+#pragma unroll
+        for (int i = 0; i < kTile; ++i) x[i] *= sl2;
       } else {
-#pragma unroll 1
+        tmax = -INFINITY;
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tmem_ld32(s_col + c * 32, x);
-          tmem_wait_ld();
           const uint32_t wc = word_of(c);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const bool vis = ((wc >> i) & 1u) && (c * 32 + i) < lim;
-            tmax = fmaxf(tmax, vis ? x[i] * sl2 : -INFINITY);
+            x[c * 32 + i] = vis ? x[c * 32 + i] * sl2 : -INFINITY;
+            tmax = fmaxf(tmax, x[c * 32 + i]);
           }
         }
       }
@@ -401,7 +437,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       }
       if (jt >= 1 && __any_sync(0xFFFFFFFFu, need)) {
         // PV_X(jt-1) is complete: the commit behind s_full covers it.
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
           tmem_ld32(o_col + c * 32, o);
@@ -411,38 +447,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
           tmem_st32(o_col + c * 32, o);
         }
       }
-      // Pass 2: P = 2^(s - m) as bf16 pairs over the S columns already read.
+      // P = 2^(s - m) as bf16 pairs over the S columns (all already read).
       const float muse = (m_run == -INFINITY) ? 0.0f : m_run;
-      float lsum = 0.0f;
-#pragma unroll 1
+      float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float x[32];
-        tmem_ld32(s_col + c * 32, x);
-        tmem_wait_ld();
         uint32_t pk[16];
-        if (full) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(x[2 * i], sl2, -muse));
-            const float p1 = ex2(fmaf(x[2 * i + 1], sl2, -muse));
-            lsum += p0 + p1;
-            pk[i] = pack_bf16(p0, p1);
-          }
-        } else {
-          const uint32_t wc = word_of(c);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int i0 = 2 * i, i1 = 2 * i + 1;
-            const bool v0ok = ((wc >> i0) & 1u) && (c * 32 + i0) < lim;
-            const bool v1ok = ((wc >> i1) & 1u) && (c * 32 + i1) < lim;
-            const float p0 = v0ok ? ex2(fmaf(x[i0], sl2, -muse)) : 0.0f;
-            const float p1 = v1ok ? ex2(fmaf(x[i1], sl2, -muse)) : 0.0f;
-            lsum += p0 + p1;
-            pk[i] = pack_bf16(p0, p1);
-          }
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(x[c * 32 + 2 * i] - muse);
+          const float p1 = ex2(x[c * 32 + 2 * i + 1] - muse);
+          ls[i & 3] += p0 + p1;
+          pk[i] = pack_bf16(p0, p1);
         }
         tmem_st16(s_col + c * 16, pk);
       }
+      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tmem_wait_st();
       l_run += lsum;
       tc_fence_before();
@@ -454,6 +474,14 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       else { fail(); sm_ok = false; }
     }
   }
+  regs_dec<kRegsLaunch>();
+  }
+  // Only once both softmax warpgroups have handed their extra registers back
+  // may the third warpgroup take its share again: setmaxnreg.inc waits
+  // without bound, so an earlier request (e.g. from the idle warps) could
+  // take registers a softmax warpgroup still needs to grow, and deadlock.
+  __syncthreads();
+  if (warp >= 8) regs_inc<kRegsLaunch>();
   const bool have_o = warp < 8 && tile_live && sm_ok && T > 0;
   if (!have_o) { m_run = -INFINITY; l_run = 0.0f; }
   // Every live tile has seen its last P V complete, so the tensor pipe and
