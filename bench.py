@@ -367,12 +367,11 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-
     import torch
     from tree_causal_verification_gb300 import jtree, synth
+    from tree_causal_verification_gb300.dist import job_throughput, max_over_ranks, rank_world
+
+    rank, world, local = rank_world()
     from tree_causal_verification_gb300.step import StepBuffers, run_step
 
     w = synth.WORKLOADS[args.workload]
@@ -419,12 +418,14 @@ def main():
     rt = _cudart()
 
     # Independent input sets, rotated so that the step's inputs exceed L2.
-    first, meta0 = make_set(w, 0, dev)
+    # Each rank is an independent replica with its own sequences (seeds).
+    seed0 = 1000 * rank
+    first, meta0 = make_set(w, seed0, dev)
     nbytes = set_bytes(first)
     R = max(1, min(16, math.ceil(2.0 * L2_BYTES / nbytes)))
     sets, metas = [first], [meta0]
     for s in range(1, R):
-        i, m = make_set(w, s, dev)
+        i, m = make_set(w, seed0 + s, dev)
         sets.append(i)
         metas.append(m)
     nodes = [sum(m["n_nodes"]) for m in metas]
@@ -520,11 +521,8 @@ def main():
         raise RuntimeError("device error flag set during the timed regions")
 
     my_nodes = sum(nodes[i % R] for i in range(K))
-    if dist:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * my_nodes / (total_ms / 1000.0)
+    value = job_throughput(my_nodes, total_ms / 1000.0, dev)   # all ranks' nodes / slowest rank
+    total_ms = max_over_ranks(total_ms, dev)
 
     # Roofline of the dominant call.
     peaks = load_peaks()
@@ -592,11 +590,8 @@ def main():
         for _ in range(e2e_steps):
             e2e_step()
         e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * e2e_steps * nodes[0] / e2e_s, "unit": UNIT,
+    e2e_value = job_throughput(e2e_steps * nodes[0], e2e_s, dev)
+    e2e = {"value": e2e_value, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
     cpu = None
