@@ -40,18 +40,25 @@ template <int K>
 struct TopK {
   float v[K];
   int i[K];
-  int n;   // real elements inserted so far (the first K always enter)
+  int n;      // real elements inserted so far (the first K always enter)
+  float thr;  // v[K-1] once K elements are in, NaN before (every test passes)
+  // Warp-wide pruning bound: the K-th best value of the warp so far (over
+  // the union of the lanes' lists). An element strictly below it ranks after
+  // K elements the warp already holds, so it cannot be in the warp's top K.
+  float wthr;
 
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int k = 0; k < K; ++k) { v[k] = -INFINITY; i[k] = INT_MAX; }
     n = 0;
+    thr = __int_as_float(0x7fffffff);
+    wthr = -INFINITY;
   }
 
   // Elements must arrive in increasing index order within a thread, so a
   // later element that ties the K-th value never displaces it.
   __device__ __forceinline__ void push(float x, int idx) {
-    if (n >= K && !(x > v[K - 1])) return;
+    if (x <= thr) return;   // false for the NaN sentinel: the first K always enter
     ++n;
     v[K - 1] = x;
     i[K - 1] = idx;
@@ -62,9 +69,8 @@ struct TopK {
         const int ti = i[k]; i[k] = i[k - 1]; i[k - 1] = ti;
       }
     }
+    if (n >= K) thr = v[K - 1];
   }
-
-  __device__ __forceinline__ float threshold() const { return n >= K ? v[K - 1] : -INFINITY; }
 };
 
 // Online log-sum-exp in log2 units: the row's running max m (of x*log2e)
@@ -134,58 +140,149 @@ __device__ __forceinline__ void warp_select(const float (&cv)[L], const int (&ci
   }
 }
 
-// Streams float4s [lo4, hi4) of `row` into per-thread state.
+// Inverse of order_key for keys of real values (key 0 = none -> -inf).
+__device__ __forceinline__ float key_value(uint32_t key) {
+  if (key == 0u) return -INFINITY;
+  const uint32_t u = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+  return __uint_as_float(u);
+}
+
+// One batch of kScanBatch float4s (element index 4*j of float4 j = j0 + u*T).
+// WARP: every lane of the warp processes a batch in this call, so the
+// warp-wide pruning bound can be refreshed.
+template <int K, bool LSE, bool WARP>
+__device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0, TopK<K>& top,
+                                           Lse& lse) {
+  float mx[kScanBatch];
+#pragma unroll
+  for (int u = 0; u < kScanBatch; ++u)
+    mx[u] = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+  if (LSE) {
+    const float bm2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * kLog2e;
+    if (bm2 > lse.m) {
+      lse.s = (lse.m == -INFINITY) ? 0.0f : lse.s * fast_ex2(lse.m - bm2);
+      lse.m = bm2;
+    }
+    if (lse.m != -INFINITY) {
+      const float nm = -lse.m;
+      float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) {
+        a0 += fast_ex2(fmaf(x[u].x, kLog2e, nm)) + fast_ex2(fmaf(x[u].y, kLog2e, nm));
+        a1 += fast_ex2(fmaf(x[u].z, kLog2e, nm)) + fast_ex2(fmaf(x[u].w, kLog2e, nm));
+      }
+      lse.s += a0 + a1;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kScanBatch; ++u) {
+    // Some element of this float4 may enter: above the lane's own K-th value
+    // and not below the warp's bound.
+    if (mx[u] >= top.wthr && !(mx[u] <= top.thr)) {
+      const int e = 4 * (j0 + u * kScanThreads);
+      top.push(x[u].x, e);
+      top.push(x[u].y, e + 1);
+      top.push(x[u].z, e + 2);
+      top.push(x[u].w, e + 3);
+    }
+  }
+  if (WARP) {
+    float wv[K];
+    int wi[K];
+    warp_select<K, K>(top.v, top.i, min(top.n, K), wv, wi);
+    top.wthr = wv[K - 1];   // -inf while the warp holds fewer than K elements
+  }
+}
+
+// Streams float4s [lo4, hi4) of `row` into per-thread state: full batches
+// without bounds checks, ping-ponging two register buffers so that one batch
+// is in flight while the other is processed, then a checked tail.
 template <int K, bool LSE>
 __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int lo4, int hi4,
                                              TopK<K>& top, Lse& lse) {
   const float4* r4 = reinterpret_cast<const float4*>(row);
   constexpr int STEP = kScanThreads * kScanBatch;
-  float4 cur[kScanBatch], nxt[kScanBatch];
-  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  int base = lo4 + (int)threadIdx.x;
+  const int tid = (int)threadIdx.x;
+  const int full_end = lo4 + ((hi4 - lo4) / STEP) * STEP;
+  float4 a[kScanBatch], b[kScanBatch];
+  int base = lo4;
+  if (base < full_end) {
 #pragma unroll
-  for (int u = 0; u < kScanBatch; ++u) {
-    const int j = base + u * kScanThreads;
-    cur[u] = (j < hi4) ? ld_stream(r4 + j) : ninf;
+    for (int u = 0; u < kScanBatch; ++u) a[u] = ld_stream(r4 + base + tid + u * kScanThreads);
   }
-  for (; base < hi4; base += STEP) {
-    // Next batch in flight while this one is processed.
+  while (base < full_end) {
+    const bool nb = base + STEP < full_end;
+    if (nb) {
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) b[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
+    }
+    scan_batch<K, LSE, true>(a, base + tid, top, lse);
+    base += STEP;
+    if (!nb) break;
+    const bool na = base + STEP < full_end;
+    if (na) {
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) a[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
+    }
+    scan_batch<K, LSE, true>(b, base + tid, top, lse);
+    base += STEP;
+    if (!na) break;
+  }
+  // Tail: fewer than STEP float4s, padded with -inf (which never enters the
+  // top-K ahead of a real element and adds 0 to the sum).
+  if (full_end < hi4) {
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u) {
-      const int j = base + STEP + u * kScanThreads;
-      nxt[u] = (j < hi4) ? ld_stream(r4 + j) : ninf;
+      const int j = full_end + tid + u * kScanThreads;
+      a[u] = j < hi4 ? ld_stream(r4 + j) : ninf;
     }
-    if (LSE) {
-      float bm = -INFINITY;
+    if (full_end + tid < hi4) {
+      // Lanes whose whole batch is padding skip it (their padding would
+      // otherwise occupy top-K slots as if they were real -inf elements).
+      float4 x[kScanBatch];
+      int cnt = 0;
 #pragma unroll
-      for (int u = 0; u < kScanBatch; ++u)
-        bm = fmaxf(bm, fmaxf(fmaxf(cur[u].x, cur[u].y), fmaxf(cur[u].z, cur[u].w)));
-      const float bm2 = bm * kLog2e;
-      if (bm2 > lse.m) {
-        lse.s = (lse.m == -INFINITY) ? 0.0f : lse.s * fast_ex2(lse.m - bm2);
-        lse.m = bm2;
+      for (int u = 0; u < kScanBatch; ++u) {
+        const int j = full_end + tid + u * kScanThreads;
+        x[u] = a[u];
+        cnt += j < hi4;
       }
-      if (lse.m != -INFINITY) {
-        float acc = 0.0f;
+      if (cnt == kScanBatch) {
+        scan_batch<K, LSE, false>(x, full_end + tid, top, lse);
+      } else {
+        // Partial batch: element-wise, in index order.
+        if (LSE) {
+          float bm = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < kScanBatch; ++u)
-          acc += fast_ex2(fmaf(cur[u].x, kLog2e, -lse.m)) + fast_ex2(fmaf(cur[u].y, kLog2e, -lse.m)) +
-                 fast_ex2(fmaf(cur[u].z, kLog2e, -lse.m)) + fast_ex2(fmaf(cur[u].w, kLog2e, -lse.m));
-        lse.s += acc;
-      }
-    }
+          for (int u = 0; u < kScanBatch; ++u)
+            if (u < cnt) bm = fmaxf(bm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+          const float bm2 = bm * kLog2e;
+          if (bm2 > lse.m) {
+            lse.s = (lse.m == -INFINITY) ? 0.0f : lse.s * fast_ex2(lse.m - bm2);
+            lse.m = bm2;
+          }
+          if (lse.m != -INFINITY) {
+            float acc = 0.0f;
 #pragma unroll
-    for (int u = 0; u < kScanBatch; ++u) {
-      const int j = base + u * kScanThreads;
-      const float4 x = cur[u];
-      const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-      if (j < hi4 && (top.n < K || mx > top.threshold())) {
-        top.push(x.x, 4 * j);
-        top.push(x.y, 4 * j + 1);
-        top.push(x.z, 4 * j + 2);
-        top.push(x.w, 4 * j + 3);
+            for (int u = 0; u < kScanBatch; ++u)
+              if (u < cnt)
+                acc += fast_ex2(fmaf(x[u].x, kLog2e, -lse.m)) + fast_ex2(fmaf(x[u].y, kLog2e, -lse.m)) +
+                       fast_ex2(fmaf(x[u].z, kLog2e, -lse.m)) + fast_ex2(fmaf(x[u].w, kLog2e, -lse.m));
+            lse.s += acc;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) {
+          if (u < cnt) {
+            const int e = 4 * (full_end + tid + u * kScanThreads);
+            top.push(x[u].x, e);
+            top.push(x[u].y, e + 1);
+            top.push(x[u].z, e + 2);
+            top.push(x[u].w, e + 3);
+          }
+        }
       }
-      cur[u] = nxt[u];
     }
   }
 }
