@@ -122,48 +122,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int g = p.g, npt = p.npt;
   const int v0 = mp * 2 * npt;
 
-  // ---- validate the sequence (same verdict in every CTA of the sequence) ----
-  const int n_raw = p.n_nodes[b];
-  const int L = p.prefix_len[b];
-  int flag = 0;
-  if (n_raw < 0 || n_raw > p.B) flag |= JT_DEVERR_NNODES;
-  if (L < 0 || L > p.Lbound) flag |= JT_DEVERR_PREFIX;
-  if (p.paged && !(flag & JT_DEVERR_PREFIX)) {
-    const int np = (L + kPageSize - 1) / kPageSize;
-    for (int i = tid; i < np; i += kThreads) {
-      const int pg = p.block_table[(size_t)b * p.max_pages + i];
-      if (pg < 0 || pg >= p.n_pages) flag |= JT_DEVERR_PAGE;
-    }
-  }
-  const int bad = __syncthreads_or(flag);
-  if (flag && rank == 0) raise_flag(p.d_err, flag);
-  const int n = bad ? 0 : n_raw;
-
-  const bool has_rows = v0 < n;
-  const bool twoB = v0 + npt < n;          // tile B holds at least one live node
-  const int p_tiles = has_rows ? (L + kTile - 1) / kTile : 0;
-  const int v_last = min(v0 + 2 * npt, n) - 1;
-  const int t_tree = has_rows ? (v_last + kTile) / kTile : 0;
-  const int t_tot = p_tiles + t_tree;
-  const int t_begin = (int)((long)rank * t_tot / S);
-  const int t_end = (int)((long)(rank + 1) * t_tot / S);
-  const int T = t_end - t_begin;
-
-  if (!has_rows) {
-    // Every row of this unit is an unused budget slot: zeros. The cluster's
-    // CTAs split the rows; no CTA of the cluster touches DSMEM.
-    const int R = 2 * kTile / S;
-    for (int i = tid; i < R * (D / 8); i += kThreads) {
-      const int r = rank * R + i / (D / 8), u = i % (D / 8);
-      const int v = v0 + r / g, j = r % g;
-      if (v < p.B)
-        reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * g + j) * D)[u] =
-            make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
-
-  // ---- set-up: barriers, TMEM ----
+  // ---- set-up (independent of the sequence's data, so it overlaps the
+  // latency of the loads below): barriers, TMEM ----
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < kStages; ++i) {
@@ -185,9 +145,51 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+
+  // ---- validate the sequence (same verdict in every CTA of the sequence) ----
+  const int n_raw = p.n_nodes[b];
+  const int L = p.prefix_len[b];
+  int flag = 0;
+  if (n_raw < 0 || n_raw > p.B) flag |= JT_DEVERR_NNODES;
+  if (L < 0 || L > p.Lbound) flag |= JT_DEVERR_PREFIX;
+  if (p.paged && !(flag & JT_DEVERR_PREFIX)) {
+    const int np = (L + kPageSize - 1) / kPageSize;
+    for (int i = tid; i < np; i += kThreads) {
+      const int pg = p.block_table[(size_t)b * p.max_pages + i];
+      if (pg < 0 || pg >= p.n_pages) flag |= JT_DEVERR_PAGE;
+    }
+  }
   tc_fence_before();
-  __syncthreads();
+  const int bad = __syncthreads_or(flag);   // also publishes the barriers and the TMEM base
   tc_fence_after();
+  if (flag && rank == 0) raise_flag(p.d_err, flag);
+  const int n = bad ? 0 : n_raw;
+
+  const bool has_rows = v0 < n;
+  const bool twoB = v0 + npt < n;          // tile B holds at least one live node
+  const int p_tiles = has_rows ? (L + kTile - 1) / kTile : 0;
+  const int v_last = min(v0 + 2 * npt, n) - 1;
+  const int t_tree = has_rows ? (v_last + kTile) / kTile : 0;
+  const int t_tot = p_tiles + t_tree;
+  const int t_begin = (int)((long)rank * t_tot / S);
+  const int t_end = (int)((long)(rank + 1) * t_tot / S);
+  const int T = t_end - t_begin;
+
+  if (!has_rows) {
+    // Every row of this unit is an unused budget slot: zeros. The cluster's
+    // CTAs split the rows; no CTA of the cluster touches DSMEM.
+    if (warp == kWarpMMA) tmem_dealloc(bars->tmem_base, kTmemCols);
+    const int R = 2 * kTile / S;
+    for (int i = tid; i < R * (D / 8); i += kThreads) {
+      const int r = rank * R + i / (D / 8), u = i % (D / 8);
+      const int v = v0 + r / g, j = r % g;
+      if (v < p.B)
+        reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * g + j) * D)[u] =
+            make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
   auto fail = [&]() {
@@ -557,40 +559,65 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   }
   if (S == 1) return;
 
-  // ---- split-KV merge: rank k finishes rows [k*RR, (k+1)*RR) of the 256 ----
+  // ---- split-KV merge: rank k finishes rows k, k+S, k+2S, ... of the 256 ----
+  // Live rows (node < n) come first in the unit, so the round-robin share
+  // spreads them evenly over the ranks; rows of unused slots are zeros.
+  constexpr int kMaxSplit = 8;
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int RR = 2 * kTile / S;
+  const int n_live = min(2 * kTile, (n - v0) * g);
   if (tid < RR) {
-    const int row = rank * RR + tid;
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, cluster.map_shared_rank(m_s, s2)[row]);
-    float lsum = 0.0f;
-    for (int s2 = 0; s2 < S; ++s2) {
-      const float ms = cluster.map_shared_rank(m_s, s2)[row];
-      const float f = (ms == -INFINITY) ? 0.0f : ex2(ms - M);
-      fac[tid * S + s2] = f;
-      lsum += f * cluster.map_shared_rank(l_s, s2)[row];
+    const int row = rank + S * tid;
+    if (row < n_live) {
+      float ms[kMaxSplit], ls[kMaxSplit];
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplit; ++s2) {
+        ms[s2] = s2 < S ? cluster.map_shared_rank(m_s, s2)[row] : -INFINITY;
+        ls[s2] = s2 < S ? cluster.map_shared_rank(l_s, s2)[row] : 0.0f;
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplit; ++s2) M = fmaxf(M, ms[s2]);
+      float lsum = 0.0f, f[kMaxSplit];
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplit; ++s2) {
+        f[s2] = (ms[s2] == -INFINITY) ? 0.0f : ex2(ms[s2] - M);
+        lsum += f[s2] * ls[s2];
+      }
+      const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplit; ++s2)
+        if (s2 < S) fac[tid * S + s2] = f[s2] * inv;
     }
-    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-    for (int s2 = 0; s2 < S; ++s2) fac[tid * S + s2] *= inv;
   }
   __syncthreads();
   for (int i = tid; i < RR * (D / 8); i += kThreads) {
     const int rl = i / (D / 8), u = i % (D / 8);
-    const int row = rank * RR + rl;
+    const int row = rank + S * rl;
     const int vv = v0 + row / g, jh = row % g;
     if (vv >= p.B) continue;
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-    if (vv < n) {
-      for (int s2 = 0; s2 < S; ++s2) {
-        const float f = fac[rl * S + s2];
-        const float4* src = reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s, s2));
-        const float4 a = src[(2 * u) * (2 * kTile) + row], c4 = src[(2 * u + 1) * (2 * kTile) + row];
-        acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
-        acc[4] += f * c4.x; acc[5] += f * c4.y; acc[6] += f * c4.z; acc[7] += f * c4.w;
+    if (row < n_live) {
+      // One half of the 8 columns at a time: all ranks' loads in flight, then the sums.
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float4 x[kMaxSplit];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplit; ++s2)
+          if (s2 < S)
+            x[s2] = reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s, s2))
+                [(2 * u + h) * (2 * kTile) + row];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSplit; ++s2) {
+          if (s2 < S) {
+            const float f = fac[rl * S + s2];
+            acc[4 * h + 0] += f * x[s2].x; acc[4 * h + 1] += f * x[s2].y;
+            acc[4 * h + 2] += f * x[s2].z; acc[4 * h + 3] += f * x[s2].w;
+          }
+        }
       }
     }
     reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[u] =
