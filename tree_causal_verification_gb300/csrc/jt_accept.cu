@@ -33,6 +33,7 @@ accept_argmax_kernel(const float* __restrict__ target, const int32_t* __restrict
   const int row = blockIdx.x / S;
   const int seg = blockIdx.x % S;
   const int b = row / (B + 1), j = row % (B + 1);
+  grid_dependency_sync();
   const int n = n_nodes[b];
   // Uniform over the cluster (same row): dead rows skip the scan entirely.
   if (n < 0 || n > B || j > n) return;
@@ -62,6 +63,7 @@ accept_walk_kernel(const int32_t* __restrict__ am, const int32_t* __restrict__ p
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * kWalkWarps + warp;
   if (b >= batch) return;
+  grid_dependency_sync();
   const int n = n_nodes[b];
   int32_t* at = acc_tokens + (size_t)b * N;
   int32_t* an = acc_nodes + (size_t)b * N;
@@ -130,6 +132,7 @@ accept_path_kernel(const float* __restrict__ target, const int32_t* __restrict__
   constexpr unsigned kFull = 0xFFFFFFFFu;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / S, rank = blockIdx.x % S;
+  grid_dependency_sync();
   const int n = n_nodes[b];
 
   // Validate and stage the tree (every CTA of the cluster reaches the same verdict).
@@ -251,24 +254,9 @@ cudaError_t launch_tree_accept(const Ctx& c, const float* target, const int32_t*
     int S = 1;
     while (S < 16 && (long)batch * S * 2 <= 4L * c.num_sms && (vocab / 4) / (2 * S) >= 1024) S *= 2;
     const int prefetch = (long)batch * B <= 64L * 64 ? 1 : 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(batch * S);
-    cfg.blockDim = dim3(kPathThreads);
-    cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = S;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (S > 8) {
-      cudaError_t e = cudaFuncSetAttribute(accept_path_kernel,
-                                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
-    return cudaLaunchKernelEx(&cfg, accept_path_kernel, target, parent, token, n_nodes, B, n_depth,
-                              vocab, S, prefetch, acc_len, acc_tokens, acc_nodes, bonus, c.d_err);
+    return launch_kernel(accept_path_kernel, dim3(batch * S), dim3(kPathThreads), 0, c.stream, S,
+                         target, parent, token, n_nodes, B, n_depth, vocab, S, prefetch, acc_len,
+                         acc_tokens, acc_nodes, bonus, c.d_err);
   }
   int32_t* am = static_cast<int32_t*>(c.workspace);
   const long rows = (long)batch * (B + 1);
@@ -276,10 +264,9 @@ cudaError_t launch_tree_accept(const Ctx& c, const float* target, const int32_t*
   cudaError_t e = launch_clustered(accept_argmax_kernel, (int)(rows * S), S, c.stream, target,
                                    n_nodes, B, vocab, S, am);
   if (e != cudaSuccess) return e;
-  accept_walk_kernel<<<(batch + kWalkWarps - 1) / kWalkWarps, kWalkWarps * 32, 0, c.stream>>>(
-      am, parent, token, n_nodes, batch, B, n_depth, vocab, acc_len, acc_tokens, acc_nodes, bonus,
-      c.d_err);
-  return cudaGetLastError();
+  return launch_kernel(accept_walk_kernel, dim3((batch + kWalkWarps - 1) / kWalkWarps),
+                       dim3(kWalkWarps * 32), 0, c.stream, 1, am, parent, token, n_nodes, batch, B,
+                       n_depth, vocab, acc_len, acc_tokens, acc_nodes, bonus, c.d_err);
 }
 
 }  // namespace jt

@@ -123,7 +123,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int v0 = mp * 2 * npt;
 
   // ---- set-up (independent of the sequence's data, so it overlaps the
-  // latency of the loads below): barriers, TMEM ----
+  // drain of the previous grid and the latency of the loads below):
+  // barriers, TMEM ----
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < kStages; ++i) {
@@ -145,6 +146,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+
+  grid_dependency_sync();
 
   // ---- validate the sequence (same verdict in every CTA of the sequence) ----
   const int n_raw = p.n_nodes[b];
@@ -706,8 +709,6 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
     S = cand;
   }
   p.S = S;
-  attr[0].val.clusterDim.x = S;
-  cfg.gridDim = dim3(units * S);
 
   CUtensorMap mq, mkc, mvc, mkt, mvt;
   const uint64_t D64 = D;
@@ -732,7 +733,8 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
       !make_map(&mvt, a.v_tree, {D64, (uint64_t)a.hkv, (uint64_t)a.B, (uint64_t)a.batch},
                 {64, 1, (uint32_t)kTile, 1}))
     return cudaErrorInvalidValue;
-  return cudaLaunchKernelEx(&cfg, kern, mq, mkc, mvc, mkt, mvt, p);
+  return launch_kernel(kern, dim3(units * S), dim3(kThreads), smem, c.stream, S, mq, mkc, mvc, mkt,
+                       mvt, p);
 }
 
 }  // namespace

@@ -42,6 +42,7 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
   const int b = blockIdx.x * (blockDim.x >> 5) + warp;
   if (b >= batch) return;  // whole warp leaves together
   constexpr unsigned kFull = 0xFFFFFFFFu;
+  grid_dependency_sync();
 
   const int nw = N * W;
   int32_t* tk = cand_s + (size_t)warp * 2 * nw;
@@ -142,16 +143,13 @@ cudaError_t launch_tree_expand(const Ctx& c, const int32_t* tok, const float* lo
   // Candidates staged per warp: 8 bytes each, at most 64 x 32 (16 KiB).
   const int warps = (size_t)n_depth * W * 8 * kWarpsPerBlock <= 44 * 1024 ? kWarpsPerBlock : 1;
   const size_t smem = (size_t)warps * n_depth * W * 8;
-  dim3 grid((batch + warps - 1) / warps), block(warps * 32);
-#define JT_EXPAND(S)                                                                        \
-  tree_expand_kernel<S><<<grid, block, smem, c.stream>>>(tok, logp, batch, n_depth, W, B,   \
-                                                          parent, token, depth, score, n_nodes)
-  if (slots <= 1) JT_EXPAND(1);
-  else if (slots <= 2) JT_EXPAND(2);
-  else if (slots <= 4) JT_EXPAND(4);
-  else JT_EXPAND(8);
-#undef JT_EXPAND
-  return cudaGetLastError();
+  const dim3 grid((batch + warps - 1) / warps), block(warps * 32);
+  auto kern = slots <= 1 ? tree_expand_kernel<1>
+            : slots <= 2 ? tree_expand_kernel<2>
+            : slots <= 4 ? tree_expand_kernel<4>
+                         : tree_expand_kernel<8>;
+  return launch_kernel(kern, grid, block, smem, c.stream, 1, tok, logp, batch, n_depth, W, B,
+                       parent, token, depth, score, n_nodes);
 }
 
 }  // namespace jt

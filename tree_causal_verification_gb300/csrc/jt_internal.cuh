@@ -38,6 +38,27 @@ __device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi)
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel of the library is launched with
+// programmatic stream serialization, so it may be scheduled while the grid
+// before it in the stream is still draining. Each kernel therefore calls
+// wait_prior_grids() before its first global-memory access (read or write),
+// which blocks until that grid has completed and its writes are visible;
+// only data-independent set-up (shared-memory barriers, TMEM allocation)
+// comes before it. Right after the wait the kernel lets its own dependent
+// grid be scheduled. On a launch without the attribute both are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void wait_prior_grids() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void release_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_sync() {
+  wait_prior_grids();
+  release_dependents();
+}
+
+// ---------------------------------------------------------------------------
 // Launch plumbing shared by jt_api.cu and the kernel files.
 // ---------------------------------------------------------------------------
 struct Ctx {
@@ -70,5 +91,37 @@ size_t attn_workspace_bytes(const jt_attn_args& a, int num_sms);
 cudaError_t launch_tree_attn(const Ctx&, const jt_attn_args& a);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Launches `kernel` on `stream` with programmatic stream serialization and,
+// when cluster > 1, 1-D clusters of `cluster` CTAs (sizes above 8 opt in to
+// non-portable clusters).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, int cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    if (cluster > 8) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace jt

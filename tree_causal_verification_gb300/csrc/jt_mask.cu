@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t* __restric
   __shared__ int32_t par_s[kMaxB];
   const int b = blockIdx.x;
   const int v = threadIdx.x;
+  grid_dependency_sync();
   const int n = n_nodes[b];
   const bool n_ok = (n >= 0 && n <= B);
   int p = -1;
@@ -61,16 +62,12 @@ cudaError_t launch_tree_mask(const Ctx& c, const int32_t* parent, const int32_t*
                              int batch, int B, uint32_t* mask) {
   if (batch == 0) return cudaSuccess;
   const int words = (B + 31) / 32;
-  dim3 grid(batch), block(B < 32 ? 32 : B);
-  if (words <= 1)
-    tree_mask_kernel<1><<<grid, block, 0, c.stream>>>(parent, n_nodes, B, mask, c.d_err);
-  else if (words <= 2)
-    tree_mask_kernel<2><<<grid, block, 0, c.stream>>>(parent, n_nodes, B, mask, c.d_err);
-  else if (words <= 4)
-    tree_mask_kernel<4><<<grid, block, 0, c.stream>>>(parent, n_nodes, B, mask, c.d_err);
-  else
-    tree_mask_kernel<8><<<grid, block, 0, c.stream>>>(parent, n_nodes, B, mask, c.d_err);
-  return cudaGetLastError();
+  const dim3 grid(batch), block(B < 32 ? 32 : B);
+  auto kern = words <= 1 ? tree_mask_kernel<1>
+            : words <= 2 ? tree_mask_kernel<2>
+            : words <= 4 ? tree_mask_kernel<4>
+                         : tree_mask_kernel<8>;
+  return launch_kernel(kern, grid, block, 0, c.stream, 1, parent, n_nodes, B, mask, c.d_err);
 }
 
 }  // namespace jt

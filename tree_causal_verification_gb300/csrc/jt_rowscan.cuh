@@ -395,23 +395,7 @@ inline int pick_row_split(long rows, int v4, int num_sms, int max_split) {
 template <typename Kernel, typename... Args>
 cudaError_t launch_clustered(Kernel kernel, int grid, int cluster, cudaStream_t stream,
                              Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kScanThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cluster > 8) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
+  return launch_kernel(kernel, dim3(grid), dim3(kScanThreads), 0, stream, cluster, args...);
 }
 
 }  // namespace jt

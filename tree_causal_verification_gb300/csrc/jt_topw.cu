@@ -31,6 +31,7 @@ topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __re
   top.init();
   Lse lse;
   lse.init();
+  grid_dependency_sync();
   scan_segment<K, true>(logits + (size_t)row * V, lo, hi, top, lse);
   block_reduce<K, true>(top, lse, &part, warp_parts);
   if (cluster_reduce<K, true>(&part, S, top, lse)) {
