@@ -66,3 +66,26 @@ def test_workspace_queries(lib):
     assert lib.jt_tree_accept_workspace_bytes(64, 16, 16, 151936) % 256 == 0
     assert lib.jt_tree_accept_workspace_bytes(64, 128, 16, 151936) == 0
     assert lib.jt_topw_workspace_bytes(1, 16, 151936, 4) == 0
+
+
+def _attn_args(batch, B, hq, hkv, D, max_prefix):
+    a = jtree.jt_attn_args(batch, B, hq, hkv, D, 0.0)
+    for f in ("q", "k_tree", "v_tree", "k_cache", "v_cache", "prefix_len", "n_nodes", "mask",
+              "out"):
+        setattr(a, f, 4096)  # never dereferenced by the query
+    a.max_prefix = max_prefix
+    return a
+
+
+def test_attn_workspace_query(lib):
+    # Few work units (one sequence, 8 KV heads, one 256-row block each): the key
+    # range is split over a cluster and the fp32 partials need scratch, bounded
+    # by one partial per SM. Many units (64 sequences x 4 KV heads x 1 block)
+    # fill the GPU without a split: no scratch.
+    small = lib.jt_tree_attn_workspace_bytes(ctypes.byref(_attn_args(1, 16, 32, 8, 128, 2048)))
+    assert small > 0 and small % 256 == 0
+    assert small <= 1024 * (256 * 128 + 1024) * 4
+    assert lib.jt_tree_attn_workspace_bytes(
+        ctypes.byref(_attn_args(64, 128, 32, 4, 128, 16384))) == 0
+    # A single key tile cannot be split.
+    assert lib.jt_tree_attn_workspace_bytes(ctypes.byref(_attn_args(1, 16, 32, 8, 128, 0))) == 0

@@ -77,9 +77,17 @@ struct AttnParams {
   const int32_t* n_nodes;
   const uint32_t* mask;
   __nv_bfloat16* out;
+  float* part;        // split-KV partials, kPartFloats per CTA (S > 1 only)
   float scale_log2;
   int32_t* d_err;
 };
+
+// Split-KV partial of one CTA in the workspace: O as [D/4][256] float4s,
+// then m[256] and l[256]. Rows are stored rank-contiguous: row R of the unit
+// at slot (R % S) * (256 / S) + R / S, so that the rows rank k finishes
+// (k, k + S, k + 2S, ...) are one contiguous run in every rank's partial.
+template <int D>
+__host__ __device__ constexpr int part_floats() { return 2 * kTile * D + 4 * kTile; }
 
 struct Bars {
   uint64_t q_full, k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
@@ -494,34 +502,43 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   __syncthreads();
 
   // ---- output (S == 1) or publish partials (S > 1); both read O from TMEM ----
-  float* o_s = reinterpret_cast<float*>(sm);                // [D/4][256] float4s over Q and the K/V ring
-  float* m_s = o_s + 2 * kTile * D;
-  float* l_s = m_s + 2 * kTile;
-  float* fac = l_s + 2 * kTile;                             // [256 / S][S]
+  const int n_live = min(2 * kTile, (n - v0) * g);   // rows of live nodes come first
   if (warp < 8) {
     const int j = R % g;
     const bool write_row = v < p.B;
     const float inv = (v < n && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
     if (S > 1) {
-      // The K/V ring and Q are dead: every PV has completed.
+      // Only rows that some rank will merge are written; coalesced per column
+      // (a warp's 32 rows land in 32 / S runs of whole 32-byte sectors). The
+      // TMEM load is warp-collective, so the whole warp takes it whenever any
+      // of its rows is live, and only the stores are per row.
+      if ((R & ~31) < n_live) {
+        const bool live = R < n_live;
+        float* part = p.part + (size_t)blockIdx.x * part_floats<D>();
+        const int slot = (R % S) * (2 * kTile / S) + R / S;
+        float4* po = reinterpret_cast<float4*>(part);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          if (have_o) {
+            tmem_ld32(o_col + c * 32, o);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        if (have_o) {
-          tmem_ld32(o_col + c * 32, o);
-          tmem_wait_ld();
-        } else {
+            for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+          }
+          if (live) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+            for (int i = 0; i < 32; i += 4)
+              __stcg(po + (c * 8 + i / 4) * (2 * kTile) + slot,
+                     make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
+          }
         }
-        // float4-column-major ([D/4][256]): consecutive rows hit consecutive banks.
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          reinterpret_cast<float4*>(o_s)[(c * 8 + i / 4) * (2 * kTile) + R] =
-              make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+        if (live) {
+          __stcg(part + 2 * kTile * D + slot, m_run);
+          __stcg(part + 2 * kTile * D + 2 * kTile + slot, l_run);
+        }
       }
-      m_s[R] = m_run;
-      l_s[R] = l_run;
     } else {
       uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * g + j) * D);
 #pragma unroll
@@ -563,21 +580,24 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   if (S == 1) return;
 
   // ---- split-KV merge: rank k finishes rows k, k+S, k+2S, ... of the 256 ----
-  // Live rows (node < n) come first in the unit, so the round-robin share
-  // spreads them evenly over the ranks; rows of unused slots are zeros.
+  // Live rows come first in the unit, so the round-robin share spreads them
+  // evenly over the ranks; rows of unused slots are zeros. The partials go
+  // through L2 (the cluster barrier orders the writes above before the
+  // reads below); every read bypasses L1.
   constexpr int kMaxSplit = 8;
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
+  cg::this_cluster().sync();
   const int RR = 2 * kTile / S;
-  const int n_live = min(2 * kTile, (n - v0) * g);
+  const float* part0 = p.part + (size_t)(blockIdx.x - rank) * part_floats<D>();
+  float* fac = reinterpret_cast<float*>(sm);                // [256 / S][S], over the dead Q tile
   if (tid < RR) {
     const int row = rank + S * tid;
     if (row < n_live) {
       float ms[kMaxSplit], ls[kMaxSplit];
 #pragma unroll
       for (int s2 = 0; s2 < kMaxSplit; ++s2) {
-        ms[s2] = s2 < S ? cluster.map_shared_rank(m_s, s2)[row] : -INFINITY;
-        ls[s2] = s2 < S ? cluster.map_shared_rank(l_s, s2)[row] : 0.0f;
+        const float* ml = part0 + (size_t)s2 * part_floats<D>() + 2 * kTile * D + rank * RR + tid;
+        ms[s2] = s2 < S ? __ldcg(ml) : -INFINITY;
+        ls[s2] = s2 < S ? __ldcg(ml + 2 * kTile) : 0.0f;
       }
       float M = -INFINITY;
 #pragma unroll
@@ -595,39 +615,31 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     }
   }
   __syncthreads();
-  for (int i = tid; i < RR * (D / 8); i += kThreads) {
-    const int rl = i / (D / 8), u = i % (D / 8);
+  // One float4 column of one row per item; a warp covers 32 consecutive
+  // slots of one column, so each of its loads is one contiguous 512-byte run.
+  for (int i = tid; i < RR * (D / 4); i += kThreads) {
+    const int rl = i % RR, c4 = i / RR;
     const int row = rank + S * rl;
     const int vv = v0 + row / g, jh = row % g;
     if (vv >= p.B) continue;
-    float acc[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (row < n_live) {
-      // One half of the 8 columns at a time: all ranks' loads in flight, then the sums.
+      const float4* src = reinterpret_cast<const float4*>(part0) + c4 * (2 * kTile) + rank * RR + rl;
+      float4 x[kMaxSplit];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float4 x[kMaxSplit];
+      for (int s2 = 0; s2 < kMaxSplit; ++s2)
+        if (s2 < S) x[s2] = __ldcg(src + (size_t)s2 * (part_floats<D>() / 4));
 #pragma unroll
-        for (int s2 = 0; s2 < kMaxSplit; ++s2)
-          if (s2 < S)
-            x[s2] = reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s, s2))
-                [(2 * u + h) * (2 * kTile) + row];
-#pragma unroll
-        for (int s2 = 0; s2 < kMaxSplit; ++s2) {
-          if (s2 < S) {
-            const float f = fac[rl * S + s2];
-            acc[4 * h + 0] += f * x[s2].x; acc[4 * h + 1] += f * x[s2].y;
-            acc[4 * h + 2] += f * x[s2].z; acc[4 * h + 3] += f * x[s2].w;
-          }
+      for (int s2 = 0; s2 < kMaxSplit; ++s2) {
+        if (s2 < S) {
+          const float f = fac[rl * S + s2];
+          acc.x += f * x[s2].x; acc.y += f * x[s2].y; acc.z += f * x[s2].z; acc.w += f * x[s2].w;
         }
       }
     }
-    reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[u] =
-        make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
-                   pack_bf16(acc[6], acc[7]));
+    reinterpret_cast<uint2*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[c4] =
+        make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
   }
-  cluster.sync();  // keep this CTA's shared memory alive until every rank has read it
 }
 
 // ---------------------------------------------------------------------------
@@ -668,6 +680,42 @@ bool make_map(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+AttnParams make_params(const jt_attn_args& a) {
+  AttnParams p = {};
+  p.batch = a.batch;
+  p.B = a.B;
+  p.hq = a.hq;
+  p.hkv = a.hkv;
+  p.g = a.hq / a.hkv;
+  p.npt = kTile / p.g;
+  p.n_mpairs = ((a.B + p.npt - 1) / p.npt + 1) / 2;
+  p.paged = a.block_table != nullptr;
+  p.max_pages = a.max_pages;
+  p.n_pages = a.n_pages;
+  p.Lbound = p.paged ? a.max_pages * kPageSize : a.max_prefix;
+  if (p.paged && a.max_prefix > 0 && a.max_prefix < p.Lbound) p.Lbound = a.max_prefix;
+  p.words = (a.B + 31) / 32;
+  p.block_table = a.block_table;
+  p.prefix_len = a.prefix_len;
+  p.n_nodes = a.n_nodes;
+  p.mask = a.mask;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  const float scale = a.scale != 0.0f ? a.scale : 1.0f / sqrtf((float)a.head_dim);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return p;
+}
+
+// Largest cluster size (power of two, at most 8) the split may use before
+// residency is checked: the grid stays within the SMs and no rank is left
+// without a key tile.
+int split_limit(const jt_attn_args& a, const AttnParams& p, int num_sms) {
+  const int units = a.batch * a.hkv * p.n_mpairs;
+  const int tiles_max = (p.Lbound + kTile - 1) / kTile + (a.B + kTile - 1) / kTile;
+  int s = 1;
+  while (s < 8 && (long)units * (2 * s) <= num_sms && 2 * s <= tiles_max) s *= 2;
+  return s;
+}
+
 template <int D>
 size_t smem_bytes() { return (2 + 2 * kStages) * (size_t)kTile * D * 2 + 256 + 1024; }
 
@@ -681,9 +729,12 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   if (e != cudaSuccess) return e;
 
   const int units = a.batch * a.hkv * p.n_mpairs;
-  const int tiles_max = (p.Lbound + kTile - 1) / kTile + (a.B + kTile - 1) / kTile;
   // Split the key tiles over a cluster only while every cluster of the grid
-  // can be resident at once (one wave) and the grid stays within the SMs.
+  // can be resident at once (one wave) and the grid stays within the SMs;
+  // the partials need the workspace sized by attn_workspace_bytes.
+  const bool have_part = p.part != nullptr &&
+                         c.workspace_bytes >= (size_t)c.num_sms * part_floats<D>() * sizeof(float);
+  const int limit = have_part ? split_limit(a, p, c.num_sms) : 1;
   int S = 1;
 
   cudaLaunchConfig_t cfg = {};
@@ -696,8 +747,7 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  for (int cand = 2; cand <= 8; cand *= 2) {
-    if (units * cand > c.num_sms || cand > tiles_max) break;
+  for (int cand = 2; cand <= limit; cand *= 2) {
     attr[0].val.clusterDim.x = cand;
     cfg.gridDim = dim3(units * cand);
     int nclusters = 0;
@@ -740,34 +790,19 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
 }  // namespace
 
 size_t attn_workspace_bytes(const jt_attn_args& a, int num_sms) {
-  (void)a;
-  (void)num_sms;
-  return 0;
+  if (a.batch == 0) return 0;
+  AttnParams p = make_params(a);
+  // A split grid never exceeds the SMs (one CTA per SM, one wave), so
+  // num_sms partials always suffice; none are needed when no split fits.
+  if (split_limit(a, p, num_sms) < 2) return 0;
+  const size_t per = (a.head_dim == 64 ? part_floats<64>() : part_floats<128>()) * sizeof(float);
+  return align_up((size_t)num_sms * per, 256);
 }
 
 cudaError_t launch_tree_attn(const Ctx& c, const jt_attn_args& a) {
   if (a.batch == 0) return cudaSuccess;
-  AttnParams p = {};
-  p.batch = a.batch;
-  p.B = a.B;
-  p.hq = a.hq;
-  p.hkv = a.hkv;
-  p.g = a.hq / a.hkv;
-  p.npt = kTile / p.g;
-  p.n_mpairs = ((a.B + p.npt - 1) / p.npt + 1) / 2;
-  p.paged = a.block_table != nullptr;
-  p.max_pages = a.max_pages;
-  p.n_pages = a.n_pages;
-  p.Lbound = p.paged ? a.max_pages * kPageSize : a.max_prefix;
-  if (p.paged && a.max_prefix > 0 && a.max_prefix < p.Lbound) p.Lbound = a.max_prefix;
-  p.words = (a.B + 31) / 32;
-  p.block_table = a.block_table;
-  p.prefix_len = a.prefix_len;
-  p.n_nodes = a.n_nodes;
-  p.mask = a.mask;
-  p.out = static_cast<__nv_bfloat16*>(a.out);
-  const float scale = a.scale != 0.0f ? a.scale : 1.0f / sqrtf((float)a.head_dim);
-  p.scale_log2 = scale * 1.4426950408889634f;
+  AttnParams p = make_params(a);
+  p.part = static_cast<float*>(c.workspace);
   p.d_err = c.d_err;
   return a.head_dim == 64 ? launch_d<64>(c, a, p) : launch_d<128>(c, a, p);
 }
