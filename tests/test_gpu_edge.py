@@ -97,6 +97,10 @@ ATTN_CASES = [
     (1, 1, [1], 2, 2, 128, [1000], False),
     (4, 48, [48, 48, 0, 20], 32, 4, 128, [127, 128, 129, 513], True),
     (2, 128, [128, 77], 8, 8, 64, [2049, 31], False),
+    # Few units and >= 16 key tiles: 16-CTA split, ragged live rows, ranks
+    # without a tile (the short second sequence).
+    (2, 24, [19, 5], 16, 2, 128, [2000, 100], False),
+    (1, 40, [37], 8, 1, 64, [2100], True),
 ]
 
 

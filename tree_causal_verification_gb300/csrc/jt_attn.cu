@@ -17,8 +17,8 @@
 // pages or contiguous) then the tree tiles holding its nodes' ancestors.
 //
 // One CTA per unit (or per slice of its key tiles when units are too few to
-// fill the GPU: split-KV over a thread-block cluster, merged in distributed
-// shared memory). 384 threads = 3 warpgroups; setmaxnreg moves registers
+// fill the GPU: split-KV over a cluster of S = 2..8 CTAs, whose fp32
+// partials meet in an L2-resident workspace across one cluster barrier). 384 threads = 3 warpgroups; setmaxnreg moves registers
 // from the third (producer / MMA, 88 each) to the two softmax warpgroups
 // (208 each) for the main loop; 384 x 168 = 256 x 208 + 128 x 88:
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread r of a
@@ -99,6 +99,85 @@ struct Bars {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 two = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&two);
+}
+
+// Split-KV merge of one unit by rank `rank` of its SS CTAs: rows
+// rank, rank + SS, rank + 2 SS, ... of the unit's 256 (live rows come first
+// in a unit, so the round-robin share spreads them evenly). Row R's result
+// is sum_s e^(m_s - M) O_s / sum_s e^(m_s - M) l_s over the SS partials,
+// M = max_s m_s (m in the log2 domain). Every partial load bypasses L1 and U
+// items are kept in flight per thread; rows of unused slots are zeros.
+template <int D, int SS, int U>
+__device__ __forceinline__ void merge_split(const AttnParams& p, const float* part0, float* fac,
+                                            int rank, int n_live, int v0, int b, int kh, int tid) {
+  constexpr int RR = 2 * kTile / SS;
+  constexpr int PF4 = part_floats<D>() / 4;
+  const int g = p.g;
+  const int nl = n_live > rank ? (n_live - rank + SS - 1) / SS : 0;   // live rows of this rank
+  if (tid < nl) {
+    const float* ml = part0 + 2 * kTile * D + rank * RR + tid;
+    float ms[SS], ls[SS];
+#pragma unroll
+    for (int s2 = 0; s2 < SS; ++s2) {
+      ms[s2] = __ldcg(ml + (size_t)s2 * part_floats<D>());
+      ls[s2] = __ldcg(ml + (size_t)s2 * part_floats<D>() + 2 * kTile);
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s2 = 0; s2 < SS; ++s2) M = fmaxf(M, ms[s2]);
+    float lsum = 0.0f, f[SS];
+#pragma unroll
+    for (int s2 = 0; s2 < SS; ++s2) {
+      f[s2] = (ms[s2] == -INFINITY) ? 0.0f : ex2(ms[s2] - M);
+      lsum += f[s2] * ls[s2];
+    }
+    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+#pragma unroll
+    for (int s2 = 0; s2 < SS; ++s2) fac[tid * SS + s2] = f[s2] * inv;
+  }
+  __syncthreads();
+  // Live rows: item i = (row rl = i % nl, float4 column c4 = i / nl); a warp
+  // reads runs of nl consecutive slots of each partial.
+  const float4* src0 = reinterpret_cast<const float4*>(part0) + rank * RR;
+  const int items = nl * (D / 4);
+  for (int i0 = tid; i0 < items; i0 += U * kThreads) {
+    float4 x[U][SS];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kThreads;
+      if (i < items) {
+        const float4* src = src0 + (i / nl) * (2 * kTile) + i % nl;
+#pragma unroll
+        for (int s2 = 0; s2 < SS; ++s2) x[u][s2] = __ldcg(src + (size_t)s2 * PF4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kThreads;
+      if (i < items) {
+        const int rl = i % nl, c4 = i / nl;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int s2 = 0; s2 < SS; ++s2) {
+          const float f = fac[rl * SS + s2];
+          acc.x += f * x[u][s2].x; acc.y += f * x[u][s2].y;
+          acc.z += f * x[u][s2].z; acc.w += f * x[u][s2].w;
+        }
+        const int row = rank + SS * rl;
+        const int vv = v0 + row / g, jh = row % g;
+        reinterpret_cast<uint2*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[c4] =
+            make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+      }
+    }
+  }
+  // Rows of unused budget slots of this rank (node < B): zeros.
+  for (int i = tid; i < (RR - nl) * (D / 8); i += kThreads) {
+    const int row = rank + SS * (nl + i / (D / 8));
+    const int vv = v0 + row / g, jh = row % g;
+    if (vv < p.B)
+      reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[i % (D / 8)] =
+          make_uint4(0, 0, 0, 0);
+  }
 }
 
 template <int D>
@@ -187,8 +266,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int T = t_end - t_begin;
 
   if (!has_rows) {
-    // Every row of this unit is an unused budget slot: zeros. The cluster's
-    // CTAs split the rows; no CTA of the cluster touches DSMEM.
+    // Every row of this unit is an unused budget slot: zeros. The unit's
+    // CTAs split the rows; with a split they still join the cluster barrier.
     if (warp == kWarpMMA) tmem_dealloc(bars->tmem_base, kTmemCols);
     const int R = 2 * kTile / S;
     for (int i = tid; i < R * (D / 8); i += kThreads) {
@@ -198,6 +277,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * g + j) * D)[u] =
             make_uint4(0, 0, 0, 0);
     }
+    if (S > 1) cg::this_cluster().sync();
     return;
   }
 
@@ -314,13 +394,18 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         mma_bf16_ts(d, a + kk * 8, v + (uint64_t)(kk * (2048 >> 4)), id_o, jt > 0 || kk > 0);
       mma_commit(&bars->pv_done[X]);
     };
-    // Rows of V past a tile's valid keys may hold anything (NaN included); P
-    // is 0 there but 0 * NaN is NaN, so they are zeroed before P V reads them.
+    // Rows of V past a tile's valid keys that the TMA read from memory may
+    // hold anything (NaN included); P is 0 there but 0 * NaN is NaN, so they
+    // are zeroed before P V reads them. Rows outside the tensor arrive as
+    // zeros already (contiguous cache past max_prefix, tree rows past B).
     auto zero_v_tail = [&](int jt) {
-      const int valid = tile_valid(t_begin + jt);
-      if (valid < kTile) {
+      const int t = t_begin + jt;
+      const int valid = tile_valid(t);
+      const int loaded = t < p_tiles ? (p.paged ? kTile : min(kTile, p.Lbound - t * kTile))
+                                     : min(kTile, p.B - (t - p_tiles) * kTile);
+      if (valid < loaded) {
         uint8_t* vt = sV(jt % kStages);
-        for (int i = lane; i < (kTile - valid) * CH * 8; i += 32) {
+        for (int i = lane; i < (loaded - valid) * CH * 8; i += 32) {
           const int r = valid + i / (CH * 8), rem = i % (CH * 8);
           *reinterpret_cast<uint4*>(vt + (rem / 8) * CHB + r * 128 + (rem % 8) * 16) =
               make_uint4(0, 0, 0, 0);
@@ -402,8 +487,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         const uint32_t w01 = (c & 1) ? ws1 : ws0, w23 = (c & 1) ? ws3 : ws2;
         return (c & 2) ? w23 : w01;
       };
-      // All 128 scores of the row at once (one wait), then mask / scale / max.
-      // A prefix tile whose 128 keys are all visible needs no per-key test.
+      // All 128 scores of the row at once (one wait), then the row max of the
+      // visible raw scores (scaling by sl2 > 0 commutes with the max; it is
+      // folded into the exponent below). A prefix tile whose 128 keys are all
+      // visible needs no per-key test; otherwise one word per 32 keys holds
+      // the visibility bits (ancestor bits and c < lim).
       const bool full = !tree && lim >= kTile;
       float x[kTile];
 #pragma unroll
@@ -414,32 +502,24 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         for (int i = 0; i < 32; ++i) x[c * 32 + i] = tmp[i];
       }
       tmem_wait_ld();
-      float tmax;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (full) {
-        float m4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-        for (int i = 4; i < kTile; i += 4) {
-          m4[0] = fmaxf(m4[0], x[i]);
-          m4[1] = fmaxf(m4[1], x[i + 1]);
-          m4[2] = fmaxf(m4[2], x[i + 2]);
-          m4[3] = fmaxf(m4[3], x[i + 3]);
-        }
-        tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;   // sl2 > 0
-#pragma unroll
-        for (int i = 0; i < kTile; ++i) x[i] *= sl2;
+        for (int i = 0; i < kTile; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
       } else {
-        tmax = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint32_t wc = word_of(c);
+          const int rem = lim - c * 32;
+          const uint32_t lim_bits = rem >= 32 ? 0xFFFFFFFFu : rem <= 0 ? 0u : (1u << rem) - 1u;
+          const uint32_t vw = word_of(c) & lim_bits;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const bool vis = ((wc >> i) & 1u) && (c * 32 + i) < lim;
-            x[c * 32 + i] = vis ? x[c * 32 + i] * sl2 : -INFINITY;
-            tmax = fmaxf(tmax, x[c * 32 + i]);
+            x[c * 32 + i] = ((vw >> i) & 1u) ? x[c * 32 + i] : -INFINITY;
+            m4[i & 3] = fmaxf(m4[i & 3], x[c * 32 + i]);
           }
         }
       }
+      const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
       const float mnew = fmaxf(m_run, tmax);
       const bool need = mnew > m_run + kRescaleLog2;
       float corr = 1.0f;
@@ -460,7 +540,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
           tmem_st32(o_col + c * 32, o);
         }
       }
-      // P = 2^(s - m) as bf16 pairs over the S columns (all already read).
+      // P = 2^(s sl2 - m) as bf16 pairs over the S columns (all already read).
       const float muse = (m_run == -INFINITY) ? 0.0f : m_run;
       float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -468,8 +548,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(x[c * 32 + 2 * i] - muse);
-          const float p1 = ex2(x[c * 32 + 2 * i + 1] - muse);
+          const float p0 = ex2(fmaf(x[c * 32 + 2 * i], sl2, -muse));
+          const float p1 = ex2(fmaf(x[c * 32 + 2 * i + 1], sl2, -muse));
           ls[i & 3] += p0 + p1;
           pk[i] = pack_bf16(p0, p1);
         }
@@ -579,66 +659,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   }
   if (S == 1) return;
 
-  // ---- split-KV merge: rank k finishes rows k, k+S, k+2S, ... of the 256 ----
-  // Live rows come first in the unit, so the round-robin share spreads them
-  // evenly over the ranks; rows of unused slots are zeros. The partials go
-  // through L2 (the cluster barrier orders the writes above before the
-  // reads below); every read bypasses L1.
-  constexpr int kMaxSplit = 8;
+  // ---- split-KV merge through L2 (the cluster barrier, reached by every CTA
+  // of the split, orders the partial writes above before the reads) ----
   cg::this_cluster().sync();
-  const int RR = 2 * kTile / S;
+  float* fac = reinterpret_cast<float*>(sm);   // over the dead Q tile
   const float* part0 = p.part + (size_t)(blockIdx.x - rank) * part_floats<D>();
-  float* fac = reinterpret_cast<float*>(sm);                // [256 / S][S], over the dead Q tile
-  if (tid < RR) {
-    const int row = rank + S * tid;
-    if (row < n_live) {
-      float ms[kMaxSplit], ls[kMaxSplit];
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxSplit; ++s2) {
-        const float* ml = part0 + (size_t)s2 * part_floats<D>() + 2 * kTile * D + rank * RR + tid;
-        ms[s2] = s2 < S ? __ldcg(ml) : -INFINITY;
-        ls[s2] = s2 < S ? __ldcg(ml + 2 * kTile) : 0.0f;
-      }
-      float M = -INFINITY;
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxSplit; ++s2) M = fmaxf(M, ms[s2]);
-      float lsum = 0.0f, f[kMaxSplit];
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxSplit; ++s2) {
-        f[s2] = (ms[s2] == -INFINITY) ? 0.0f : ex2(ms[s2] - M);
-        lsum += f[s2] * ls[s2];
-      }
-      const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxSplit; ++s2)
-        if (s2 < S) fac[tid * S + s2] = f[s2] * inv;
-    }
-  }
-  __syncthreads();
-  // One float4 column of one row per item; a warp covers 32 consecutive
-  // slots of one column, so each of its loads is one contiguous 512-byte run.
-  for (int i = tid; i < RR * (D / 4); i += kThreads) {
-    const int rl = i % RR, c4 = i / RR;
-    const int row = rank + S * rl;
-    const int vv = v0 + row / g, jh = row % g;
-    if (vv >= p.B) continue;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (row < n_live) {
-      const float4* src = reinterpret_cast<const float4*>(part0) + c4 * (2 * kTile) + rank * RR + rl;
-      float4 x[kMaxSplit];
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxSplit; ++s2)
-        if (s2 < S) x[s2] = __ldcg(src + (size_t)s2 * (part_floats<D>() / 4));
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxSplit; ++s2) {
-        if (s2 < S) {
-          const float f = fac[rl * S + s2];
-          acc.x += f * x[s2].x; acc.y += f * x[s2].y; acc.z += f * x[s2].z; acc.w += f * x[s2].w;
-        }
-      }
-    }
-    reinterpret_cast<uint2*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[c4] =
-        make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  switch (S) {
+    case 2: merge_split<D, 2, 4>(p, part0, fac, rank, n_live, v0, b, kh, tid); break;
+    case 4: merge_split<D, 4, 2>(p, part0, fac, rank, n_live, v0, b, kh, tid); break;
+    default: merge_split<D, 8, 1>(p, part0, fac, rank, n_live, v0, b, kh, tid); break;
   }
 }
 
@@ -705,9 +734,8 @@ AttnParams make_params(const jt_attn_args& a) {
   return p;
 }
 
-// Largest cluster size (power of two, at most 8) the split may use before
-// residency is checked: the grid stays within the SMs and no rank is left
-// without a key tile.
+// Largest split (power of two, at most 8) before residency is checked: the
+// grid stays within the SMs and no rank is left without a key tile.
 int split_limit(const jt_attn_args& a, const AttnParams& p, int num_sms) {
   const int units = a.batch * a.hkv * p.n_mpairs;
   const int tiles_max = (p.Lbound + kTile - 1) / kTile + (a.B + kTile - 1) / kTile;
@@ -725,33 +753,29 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   auto kern = tree_attn_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
 
   const int units = a.batch * a.hkv * p.n_mpairs;
-  // Split the key tiles over a cluster only while every cluster of the grid
-  // can be resident at once (one wave) and the grid stays within the SMs;
-  // the partials need the workspace sized by attn_workspace_bytes.
+  // Split the key tiles over S CTAs only when the workspace holds the partials.
   const bool have_part = p.part != nullptr &&
                          c.workspace_bytes >= (size_t)c.num_sms * part_floats<D>() * sizeof(float);
   const int limit = have_part ? split_limit(a, p, c.num_sms) : 1;
+  // Largest split whose clusters are all resident at once (one wave).
   int S = 1;
-
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = c.stream;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t occ = {};
+  cudaLaunchAttribute occ_attr[1];
+  occ.blockDim = dim3(kThreads);
+  occ.dynamicSmemBytes = smem;
+  occ.stream = c.stream;
+  occ_attr[0].id = cudaLaunchAttributeClusterDimension;
+  occ_attr[0].val.clusterDim.y = 1;
+  occ_attr[0].val.clusterDim.z = 1;
+  occ.attrs = occ_attr;
+  occ.numAttrs = 1;
   for (int cand = 2; cand <= limit; cand *= 2) {
-    attr[0].val.clusterDim.x = cand;
-    cfg.gridDim = dim3(units * cand);
+    occ_attr[0].val.clusterDim.x = cand;
+    occ.gridDim = dim3(units * cand);
     int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &occ) != cudaSuccess) {
       cudaGetLastError();
       break;
     }
