@@ -148,11 +148,12 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 }
 
 // One batch of kScanBatch float4s (element index 4*j of float4 j = j0 + u*T).
-// WARP: every lane of the warp processes a batch in this call, so the
-// warp-wide pruning bound can be refreshed.
-template <int K, bool LSE, bool WARP>
+// refresh: every lane of the warp processes a batch in this call and the
+// warp-wide pruning bound is recomputed afterwards (K rounds of warp argmax,
+// so it is done only while the bound is still tightening quickly).
+template <int K, bool LSE>
 __device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0, TopK<K>& top,
-                                           Lse& lse) {
+                                           Lse& lse, bool refresh) {
   float mx[kScanBatch];
 #pragma unroll
   for (int u = 0; u < kScanBatch; ++u)
@@ -186,7 +187,7 @@ __device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0
       top.push(x[u].w, e + 3);
     }
   }
-  if (WARP) {
+  if (refresh) {
     float wv[K];
     int wi[K];
     warp_select<K, K>(top.v, top.i, min(top.n, K), wv, wi);
@@ -206,6 +207,10 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
   const int full_end = lo4 + ((hi4 - lo4) / STEP) * STEP;
   float4 a[kScanBatch], b[kScanBatch];
   int base = lo4;
+  // Full batches are uniform over the CTA; the warp bound is refreshed after
+  // batches 1, 2, 4, 8, ... (a stale bound is still a valid, looser bound).
+  int nbatch = 0;
+  auto refresh = [&]() { ++nbatch; return (nbatch & (nbatch - 1)) == 0; };
   if (base < full_end) {
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u) a[u] = ld_stream(r4 + base + tid + u * kScanThreads);
@@ -216,7 +221,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) b[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
     }
-    scan_batch<K, LSE, true>(a, base + tid, top, lse);
+    scan_batch<K, LSE>(a, base + tid, top, lse, refresh());
     base += STEP;
     if (!nb) break;
     const bool na = base + STEP < full_end;
@@ -224,7 +229,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) a[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
     }
-    scan_batch<K, LSE, true>(b, base + tid, top, lse);
+    scan_batch<K, LSE>(b, base + tid, top, lse, refresh());
     base += STEP;
     if (!na) break;
   }
@@ -249,7 +254,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
         cnt += j < hi4;
       }
       if (cnt == kScanBatch) {
-        scan_batch<K, LSE, false>(x, full_end + tid, top, lse);
+        scan_batch<K, LSE>(x, full_end + tid, top, lse, false);
       } else {
         // Partial batch: element-wise, in index order.
         if (LSE) {
