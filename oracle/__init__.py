@@ -58,8 +58,12 @@ def _load():
                                             ctypes.c_int, _i32p, _i32p, _i32p, _f32p, _i32p]
             lib.orc_tree_accept.argtypes = [_f32p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_int, _i32p, _i32p, _i32p, _i32p]
+            lib.orc_tree_commit_kv.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                _u16p, _u16p, _u16p, _u16p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, _i32p, _i32p, _i32p, _i32p]
             for f in (lib.orc_tree_mask, lib.orc_tree_attn, lib.orc_topw, lib.orc_tree_expand,
-                      lib.orc_tree_accept):
+                      lib.orc_tree_accept, lib.orc_tree_commit_kv):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -191,3 +195,36 @@ def tree_accept(target, parent, token, n_nodes, n_depth):
                                    _ptr(acc_nodes, _i32p), _ptr(bonus, _i32p)),
            "orc_tree_accept")
     return dict(acc_len=acc_len, acc_tokens=acc_tokens, acc_nodes=acc_nodes, bonus=bonus)
+
+
+def tree_commit_kv(k_tree, v_tree, k_cache, v_cache, prefix_len, acc_len, acc_nodes,
+                   block_table=None, check=True):
+    """Append the accepted path's tree K/V rows to the prefix cache.
+
+    k/v_tree [batch][B][hkv][D] and k/v_cache (contiguous [batch][Lmax][hkv][D]
+    or paged [pages][page_size][hkv][D]) as bf16 bit patterns (uint16) or
+    torch bf16. Returns (k_cache', v_cache', new_prefix_len, rc) on copies;
+    the inputs are not modified. check=False returns the oracle's status
+    instead of raising on rejected sequences.
+    """
+    k_tree, v_tree = _bf16_bits(k_tree), _bf16_bits(v_tree)
+    k_out, v_out = _bf16_bits(k_cache).copy(), _bf16_bits(v_cache).copy()
+    prefix_len = _arr(prefix_len, np.int32)
+    acc_len = _arr(acc_len, np.int32)
+    acc_nodes = _arr(acc_nodes, np.int32)
+    batch, B, hkv, D = k_tree.shape
+    n_depth = acc_nodes.shape[1]
+    if block_table is not None:
+        block_table = _arr(block_table, np.int32)
+        max_pages, page_size, n_pool, max_prefix = block_table.shape[1], k_out.shape[1], k_out.shape[0], 0
+    else:
+        max_pages, page_size, n_pool, max_prefix = 0, 0, 0, k_out.shape[1]
+    new_len = np.zeros((batch,), np.int32)
+    rc = _load().orc_tree_commit_kv(batch, B, n_depth, hkv, D, _ptr(k_tree, _u16p),
+                                    _ptr(v_tree, _u16p), _ptr(k_out, _u16p), _ptr(v_out, _u16p),
+                                    _ptr(block_table, _i32p), page_size, max_pages, n_pool,
+                                    max_prefix, _ptr(prefix_len, _i32p), _ptr(acc_len, _i32p),
+                                    _ptr(acc_nodes, _i32p), _ptr(new_len, _i32p))
+    if check:
+        _check(rc, "orc_tree_commit_kv")
+    return k_out, v_out, new_len, rc

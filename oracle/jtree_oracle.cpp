@@ -13,6 +13,7 @@
 //   orc_topw         - full stable sort of the vocabulary + fp64 log-softmax
 //   orc_tree_expand  - best-first expansion on a std::priority_queue
 //   orc_tree_accept  - sequential argmax + walk down the tree
+//   orc_tree_commit_kv - append the accepted path's K/V rows to the prefix cache
 //
 // Sources (page title, site, section):
 //   [PL]  "JetSpec: Breaking the Scaling Ceiling of Speculative Decoding with
@@ -353,6 +354,73 @@ int orc_tree_accept(const float* target, const int32_t* parent, const int32_t* t
     bonus[b] = a;
   }
   return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Accepted-path K/V commit. [PP] §3 "Preliminaries": a verification round
+// commits the accepted prefix plus one bonus token. The accepted draft nodes'
+// K/V were produced by the verification pass (they are rows of the tree K/V),
+// so committing them appends those rows to the sequence's prefix cache in path
+// order. The bonus token has no K/V yet (the next round computes it when it
+// verifies that token as its root), so it is not written.
+//
+// For sequence b with L = prefix_len[b] and a = acc_len[b]:
+//   cache position L + i  <-  tree row acc_nodes[b][i], for i = 0 .. a-1
+//                             (every KV head, K and V)
+//   new_prefix_len[b] = L + a
+// Layouts as in orc_tree_attn (elements are bf16 bit patterns). A sequence is
+// left untouched, with new_prefix_len[b] = L, when a is outside [0, n_depth],
+// an accepted node is outside [0, B), L is negative, L + a exceeds the cache
+// (max_prefix, or max_pages * page_size when paged), or a page id it would
+// write is outside [0, n_pool_pages); the call then returns kBadTree after
+// processing every sequence. new_prefix_len may alias prefix_len.
+// ---------------------------------------------------------------------------
+int orc_tree_commit_kv(int batch, int B, int n_depth, int hkv, int D,
+                       const uint16_t* k_tree, const uint16_t* v_tree,
+                       uint16_t* k_cache, uint16_t* v_cache,
+                       const int32_t* block_table, int page_size, int max_pages,
+                       int n_pool_pages, int max_prefix,
+                       const int32_t* prefix_len, const int32_t* acc_len,
+                       const int32_t* acc_nodes, int32_t* new_prefix_len) {
+  if (batch < 0 || B <= 0 || n_depth <= 0 || hkv <= 0 || D <= 0) return kBadArg;
+  if (block_table && (page_size <= 0 || max_pages <= 0)) return kBadArg;
+  const size_t row = static_cast<size_t>(hkv) * D;   // elements per token row
+  const long capacity = block_table ? static_cast<long>(max_pages) * page_size : max_prefix;
+  int rc = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int L = prefix_len[b];
+    const int a = acc_len[b];
+    const int32_t* path = acc_nodes + static_cast<size_t>(b) * n_depth;
+    bool ok = L >= 0 && a >= 0 && a <= n_depth && static_cast<long>(L) + a <= capacity;
+    for (int i = 0; ok && i < a; ++i)
+      if (path[i] < 0 || path[i] >= B) ok = false;
+    // Where each committed token goes: its cache row index (element offset / row).
+    std::vector<size_t> dst(ok ? a : 0);
+    for (int i = 0; ok && i < a; ++i) {
+      const long pos = static_cast<long>(L) + i;
+      if (block_table) {
+        const int page = block_table[static_cast<size_t>(b) * max_pages + pos / page_size];
+        if (page < 0 || page >= n_pool_pages) { ok = false; break; }
+        dst[i] = static_cast<size_t>(page) * page_size + pos % page_size;
+      } else {
+        dst[i] = static_cast<size_t>(b) * max_prefix + pos;
+      }
+    }
+    if (!ok) {
+      rc = kBadTree;
+      new_prefix_len[b] = L;
+      continue;
+    }
+    for (int i = 0; i < a; ++i) {
+      const size_t src = (static_cast<size_t>(b) * B + path[i]) * row;
+      for (size_t e = 0; e < row; ++e) {
+        k_cache[dst[i] * row + e] = k_tree[src + e];
+        v_cache[dst[i] * row + e] = v_tree[src + e];
+      }
+    }
+    new_prefix_len[b] = L + a;
+  }
+  return rc;
 }
 
 }  // extern "C"
