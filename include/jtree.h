@@ -1,8 +1,8 @@
 /*
  * libjtree — one decode step of causal parallel tree drafting (JetSpec) on a
  * GB300 (sm_103a): per-depth top-W candidates, best-first tree expansion,
- * the tree-causal mask, tree attention for the verification pass, and greedy
- * acceptance.
+ * the tree-causal mask, tree attention for the verification pass, greedy
+ * acceptance, and the commit of the accepted path's K/V into the prefix cache.
  *
  * Sources (page title, site, section):
  *   [PL] "JetSpec: Breaking the Scaling Ceiling of Speculative Decoding with
@@ -74,6 +74,7 @@ typedef enum {
 #define JT_DEVERR_PAGE     0x08  /* a block-table page id outside the pool */
 #define JT_DEVERR_PREFIX   0x10  /* prefix_len outside [0, max_prefix] */
 #define JT_DEVERR_TIMEOUT  0x20  /* a bounded wait on an mbarrier ran out */
+#define JT_DEVERR_PATH     0x40  /* acc_len outside [0, n_depth] or an accepted node outside [0, B) */
 
 typedef struct {
   jt_stream_t stream;       /* stream every launch is enqueued on (NULL = default) */
@@ -258,6 +259,56 @@ JT_API jt_status jt_tree_accept_noalloc(const float* target_logits, const int32_
                                         int B, int n_depth, int vocab, int32_t* acc_len,
                                         int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus,
                                         const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
+ * jt_tree_commit_kv — append the accepted path's K/V to the prefix cache.
+ * [PP] §3 "Preliminaries": a verification round commits the accepted prefix
+ * plus one bonus token. The accepted draft nodes' K/V were produced by the
+ * verification pass (rows of k_tree / v_tree), so committing them copies
+ * those rows into the cache after the prefix, in path order. The bonus
+ * token has no K/V yet (the next round produces it when it verifies that
+ * token as its root) and is not written.
+ *
+ * For sequence b with L = prefix_len[b], a = acc_len[b] (from jt_tree_accept):
+ *   cache position L + i  <-  tree row acc_nodes[b][i], i = 0 .. a-1, for
+ *                              every KV head, K and V
+ *   new_prefix_len[b] = L + a
+ *
+ *   k_tree, v_tree  bf16 [batch][B][hkv][D]        read only
+ *   k_cache, v_cache: contiguous (block_table == NULL) bf16
+ *                   [batch][max_prefix][hkv][D]; paged: pool
+ *                   [n_pages][page_size][hkv][D] with block_table int32
+ *                   [batch][max_pages] (token j of sequence b in page
+ *                   block_table[b][j / page_size], slot j % page_size).
+ *                   Only the committed slots are written.
+ *   prefix_len      int32 [batch]
+ *   acc_len         int32 [batch], acc_nodes int32 [batch][n_depth]
+ *   new_prefix_len  int32 [batch]; may alias prefix_len (the call reads every
+ *                   length before writing any)
+ * Limits: 1 <= B <= 256, 1 <= n_depth <= 64, hkv >= 1, head_dim % 8 == 0,
+ * hkv * head_dim <= 4096, page_size == 16 when paged. No workspace.
+ * Device checks: a outside [0, n_depth] or an accepted node outside [0, B)
+ * (JT_DEVERR_PATH), L < 0 or L + a beyond the cache (max_prefix, or
+ * max_pages * page_size) (JT_DEVERR_PREFIX), a page id outside [0, n_pages)
+ * among the slots to write (JT_DEVERR_PAGE): that sequence is left untouched
+ * and new_prefix_len[b] = L.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int batch, B, n_depth, hkv, head_dim;
+  const void* k_tree;
+  const void* v_tree;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* block_table;   /* NULL = contiguous cache */
+  int page_size, max_pages, n_pages;
+  int max_prefix;               /* contiguous: positions per sequence */
+  const int32_t* prefix_len;
+  const int32_t* acc_len;
+  const int32_t* acc_nodes;
+  int32_t* new_prefix_len;
+} jt_commit_args;
+
+JT_API jt_status jt_tree_commit_kv(const jt_commit_args* args, const jt_exec* exec);
 
 #ifdef __cplusplus
 }

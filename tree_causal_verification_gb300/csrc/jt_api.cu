@@ -167,6 +167,29 @@ jt_status jt_tree_attn(const jt_attn_args* args, const jt_exec* exec) {
   return from_cuda(launch_tree_attn(c, *args));
 }
 
+jt_status jt_tree_commit_kv(const jt_commit_args* a, const jt_exec* exec) {
+  if (!a) return JT_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->B < 1 || a->B > kMaxB || a->n_depth < 1 || a->n_depth > kMaxDepth ||
+      a->hkv < 1 || a->head_dim < 1 || (long)a->hkv * a->head_dim > 4096)
+    return JT_ERR_INVALID_ARG;
+  if (a->head_dim % 8 != 0) return JT_ERR_UNSUPPORTED;
+  const void* ptrs[] = {a->k_tree, a->v_tree, a->k_cache, a->v_cache, a->prefix_len,
+                        a->acc_len, a->acc_nodes, a->new_prefix_len};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return JT_ERR_INVALID_ARG;
+  if (a->block_table) {
+    if (!aligned16(a->block_table)) return JT_ERR_INVALID_ARG;
+    if (a->page_size != kPageSize) return JT_ERR_UNSUPPORTED;
+    if (a->max_pages < 1 || a->n_pages < 1) return JT_ERR_INVALID_ARG;
+  } else if (a->max_prefix < 0) {
+    return JT_ERR_INVALID_ARG;
+  }
+  Ctx c;
+  jt_status st = make_ctx(exec, &c);
+  if (st != JT_OK) return st;
+  return from_cuda(launch_tree_commit(c, *a));
+}
+
 size_t jt_tree_accept_workspace_bytes(int batch, int B, int n_depth, int vocab) {
   if (batch < 0 || B < 1 || B > kMaxB || n_depth < 1 || n_depth > kMaxDepth || vocab < 1) return 0;
   return accept_workspace_bytes(batch, B, n_depth, vocab);

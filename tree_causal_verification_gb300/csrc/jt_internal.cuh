@@ -87,6 +87,7 @@ cudaError_t launch_tree_accept(const Ctx&, const float* target, const int32_t* p
                                const int32_t* token, const int32_t* n_nodes, int batch, int B,
                                int n_depth, int vocab, int32_t* acc_len, int32_t* acc_tokens,
                                int32_t* acc_nodes, int32_t* bonus);
+cudaError_t launch_tree_commit(const Ctx&, const jt_commit_args& a);
 size_t attn_workspace_bytes(const jt_attn_args& a, int num_sms);
 cudaError_t launch_tree_attn(const Ctx&, const jt_attn_args& a);
 

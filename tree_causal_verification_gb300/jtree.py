@@ -27,12 +27,14 @@ JT_DEVERR_NNODES = 0x04
 JT_DEVERR_PAGE = 0x08
 JT_DEVERR_PREFIX = 0x10
 JT_DEVERR_TIMEOUT = 0x20
+JT_DEVERR_PATH = 0x40
 STATUS_NAMES = {0: "JT_OK", 1: "JT_ERR_INVALID_ARG", 2: "JT_ERR_UNSUPPORTED", 3: "JT_ERR_CUDA",
                 4: "JT_ERR_DEVICE_DATA", 5: "JT_ERR_TIMEOUT", 6: "JT_ERR_WORKSPACE"}
 
 EXPORTED = ["jt_status_str", "jt_read_device_error", "jt_topw_workspace_bytes", "jt_topw",
             "jt_tree_expand", "jt_tree_mask", "jt_tree_attn_workspace_bytes", "jt_tree_attn",
-            "jt_tree_accept_workspace_bytes", "jt_tree_accept", "jt_tree_accept_noalloc"]
+            "jt_tree_accept_workspace_bytes", "jt_tree_accept", "jt_tree_accept_noalloc",
+            "jt_tree_commit_kv"]
 
 
 class JtError(RuntimeError):
@@ -56,6 +58,18 @@ class jt_attn_args(ctypes.Structure):
                 ("max_pages", ctypes.c_int), ("n_pages", ctypes.c_int),
                 ("max_prefix", ctypes.c_int), ("prefix_len", ctypes.c_void_p),
                 ("n_nodes", ctypes.c_void_p), ("mask", ctypes.c_void_p), ("out", ctypes.c_void_p)]
+
+
+class jt_commit_args(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("B", ctypes.c_int), ("n_depth", ctypes.c_int),
+                ("hkv", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("k_tree", ctypes.c_void_p), ("v_tree", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int),
+                ("max_pages", ctypes.c_int), ("n_pages", ctypes.c_int),
+                ("max_prefix", ctypes.c_int), ("prefix_len", ctypes.c_void_p),
+                ("acc_len", ctypes.c_void_p), ("acc_nodes", ctypes.c_void_p),
+                ("new_prefix_len", ctypes.c_void_p)]
 
 
 _lib = None
@@ -90,8 +104,10 @@ def load(path: str = LIB_PATH):
             lib.jt_tree_accept.argtypes = [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                            _vp, _vp, _vp, _vp, _pexec]
             lib.jt_tree_accept_noalloc.argtypes = lib.jt_tree_accept.argtypes
+            lib.jt_tree_commit_kv.argtypes = [ctypes.POINTER(jt_commit_args), _pexec]
             for name in ("jt_read_device_error", "jt_topw", "jt_tree_expand", "jt_tree_mask",
-                         "jt_tree_attn", "jt_tree_accept", "jt_tree_accept_noalloc"):
+                         "jt_tree_attn", "jt_tree_accept", "jt_tree_accept_noalloc",
+                         "jt_tree_commit_kv"):
                 getattr(lib, name).restype = _c_int
             _lib = lib
     return _lib
@@ -318,3 +334,42 @@ def jt_tree_accept_noalloc(target, parent, token, n_nodes, n_depth, out=None, ex
                                          _ptr(out["bonus"]), ctypes.byref(c)),
            "jt_tree_accept_noalloc")
     return out
+
+
+def commit_args(k_tree, v_tree, k_cache, v_cache, prefix_len, acc_len, acc_nodes, new_prefix_len,
+                block_table=None) -> jt_commit_args:
+    batch, B, hkv, D = k_tree.shape
+    n_depth = acc_nodes.shape[1]
+    _need(k_tree, torch.bfloat16, (batch, B, hkv, D), "k_tree")
+    _need(v_tree, torch.bfloat16, (batch, B, hkv, D), "v_tree")
+    _need(prefix_len, torch.int32, (batch,), "prefix_len")
+    _need(acc_len, torch.int32, (batch,), "acc_len")
+    _need(acc_nodes, torch.int32, (batch, n_depth), "acc_nodes")
+    _need(new_prefix_len, torch.int32, (batch,), "new_prefix_len")
+    if block_table is not None:
+        n_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+        _need(k_cache, torch.bfloat16, (n_pages, page_size, hkv, D), "k_cache")
+        _need(v_cache, torch.bfloat16, (n_pages, page_size, hkv, D), "v_cache")
+        _need(block_table, torch.int32, (batch, block_table.shape[1]), "block_table")
+        max_pages, mp = block_table.shape[1], 0
+    else:
+        Lmax = k_cache.shape[1]
+        _need(k_cache, torch.bfloat16, (batch, Lmax, hkv, D), "k_cache")
+        _need(v_cache, torch.bfloat16, (batch, Lmax, hkv, D), "v_cache")
+        n_pages, page_size, max_pages, mp = 0, 0, 0, Lmax
+    return jt_commit_args(batch, B, n_depth, hkv, D, _ptr(k_tree), _ptr(v_tree), _ptr(k_cache),
+                          _ptr(v_cache), _ptr(block_table), page_size, max_pages, n_pages, mp,
+                          _ptr(prefix_len), _ptr(acc_len), _ptr(acc_nodes), _ptr(new_prefix_len))
+
+
+def jt_tree_commit_kv(k_tree, v_tree, k_cache, v_cache, prefix_len, acc_len, acc_nodes,
+                      new_prefix_len=None, block_table=None, exec=None):
+    """Writes the accepted path's tree K/V rows into k_cache / v_cache (in place)
+    after each sequence's prefix; returns new_prefix_len (int32 [batch])."""
+    if new_prefix_len is None:
+        new_prefix_len = torch.empty_like(prefix_len)
+    args = commit_args(k_tree, v_tree, k_cache, v_cache, prefix_len, acc_len, acc_nodes,
+                       new_prefix_len, block_table)
+    c = _exec(exec).c()
+    _check(load().jt_tree_commit_kv(ctypes.byref(args), ctypes.byref(c)), "jt_tree_commit_kv")
+    return new_prefix_len
