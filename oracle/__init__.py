@@ -58,12 +58,17 @@ def _load():
                                             ctypes.c_int, _i32p, _i32p, _i32p, _f32p, _i32p]
             lib.orc_tree_accept.argtypes = [_f32p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_int, _i32p, _i32p, _i32p, _i32p]
+            lib.orc_row_entropy.argtypes = [_f32p, ctypes.c_long, ctypes.c_int, _f32p]
+            lib.orc_tree_expand_scored.argtypes = [
+                _i32p, _f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_float, _i32p, _i32p, _i32p, _f32p, _i32p]
             lib.orc_tree_commit_kv.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _u16p, _u16p, _u16p, _u16p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, _i32p, _i32p, _i32p, _i32p]
             for f in (lib.orc_tree_mask, lib.orc_tree_attn, lib.orc_topw, lib.orc_tree_expand,
-                      lib.orc_tree_accept, lib.orc_tree_commit_kv):
+                      lib.orc_tree_accept, lib.orc_tree_commit_kv, lib.orc_row_entropy,
+                      lib.orc_tree_expand_scored):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -160,20 +165,38 @@ def topw(logits, W):
     return tok, logp
 
 
-def tree_expand(tok, logp, B):
-    """Best-first expansion -> dict(parent, token, depth, score, n_nodes)."""
+def tree_expand(tok, logp, B, entropy=None, mode=0, alpha=0.0):
+    """Best-first expansion -> dict(parent, token, depth, score, n_nodes).
+
+    mode 0: cumulative log-prob; 1: hybrid (increment logp - alpha*H_d);
+    2: entropy only (increment -H_d). entropy: fp32 [batch][n_depth]."""
     tok = _arr(tok, np.int32)
     logp = _arr(logp, np.float32)
     batch, n_depth, W = tok.shape
+    if entropy is not None:
+        entropy = _arr(entropy, np.float32)
+        assert entropy.shape == (batch, n_depth)
     parent = np.zeros((batch, B), np.int32)
     token = np.zeros((batch, B), np.int32)
     depth = np.zeros((batch, B), np.int32)
     score = np.zeros((batch, B), np.float32)
     n_nodes = np.zeros((batch,), np.int32)
-    _check(_load().orc_tree_expand(_ptr(tok, _i32p), _ptr(logp, _f32p), batch, n_depth, W, B,
-                                   _ptr(parent, _i32p), _ptr(token, _i32p), _ptr(depth, _i32p),
-                                   _ptr(score, _f32p), _ptr(n_nodes, _i32p)), "orc_tree_expand")
+    _check(_load().orc_tree_expand_scored(_ptr(tok, _i32p), _ptr(logp, _f32p),
+                                          _ptr(entropy, _f32p), batch, n_depth, W, B, int(mode),
+                                          float(alpha), _ptr(parent, _i32p), _ptr(token, _i32p),
+                                          _ptr(depth, _i32p), _ptr(score, _f32p),
+                                          _ptr(n_nodes, _i32p)), "orc_tree_expand_scored")
     return dict(parent=parent, token=token, depth=depth, score=score, n_nodes=n_nodes)
+
+
+def row_entropy(rows):
+    """Shannon entropy (nats) of softmax over the last axis, fp64 -> fp32."""
+    rows = _arr(rows, np.float32)
+    V = rows.shape[-1]
+    out = np.zeros(rows.shape[:-1], np.float32)
+    _check(_load().orc_row_entropy(_ptr(rows, _f32p), int(np.prod(rows.shape[:-1])), V,
+                                   _ptr(out, _f32p)), "orc_row_entropy")
+    return out
 
 
 def tree_accept(target, parent, token, n_nodes, n_depth):

@@ -11,7 +11,9 @@
 //   orc_tree_mask    - the tree-causal mask M[v,u] (explicit ancestor walk)
 //   orc_tree_attn    - attention with an explicit dense mask, fp64 softmax
 //   orc_topw         - full stable sort of the vocabulary + fp64 log-softmax
+//   orc_row_entropy  - fp64 Shannon entropy of softmax(row), in nats
 //   orc_tree_expand  - best-first expansion on a std::priority_queue
+//                      (orc_tree_expand_scored: hybrid / entropy-only scores)
 //   orc_tree_accept  - sequential argmax + walk down the tree
 //   orc_tree_commit_kv - append the accepted path's K/V rows to the prefix cache
 //
@@ -236,6 +238,36 @@ int orc_topw(const float* logits, int batch, int n_depth, int vocab, int W,
 }
 
 // ---------------------------------------------------------------------------
+// Per-depth entropy of the draft distribution. [PL] App. C "Tree-Drafting
+// Algorithm Ablation" and App. E "Drafting": besides cumulative log-prob the
+// proposer supports entropy-guided and hybrid scores built from the per-depth
+// (marginal) entropy of the draft distribution.
+//   H = -sum_j p_j ln p_j,  p = softmax(row)   (nats)
+// computed in double as ln Z - sum_j (x_j - m) e^(x_j - m) / Z with m the row
+// max and Z = sum_j e^(x_j - m); -inf logits contribute nothing (p ln p -> 0).
+// A row of all -inf has no distribution; its entropy is reported as 0.
+// ---------------------------------------------------------------------------
+int orc_row_entropy(const float* rows, long n_rows, int vocab, float* entropy) {
+  if (n_rows < 0 || vocab <= 0) return kBadArg;
+  for (long r = 0; r < n_rows; ++r) {
+    const float* x = rows + r * vocab;
+    double m = -std::numeric_limits<double>::infinity();
+    for (int j = 0; j < vocab; ++j) m = std::max(m, static_cast<double>(x[j]));
+    if (m == -std::numeric_limits<double>::infinity()) { entropy[r] = 0.0f; continue; }
+    double z = 0.0, s = 0.0;
+    for (int j = 0; j < vocab; ++j) {
+      if (x[j] == -std::numeric_limits<float>::infinity()) continue;
+      const double d = static_cast<double>(x[j]) - m;
+      const double e = std::exp(d);
+      z += e;
+      s += d * e;
+    }
+    entropy[r] = static_cast<float>(std::log(z) - s / z);
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
 // Best-first tree expansion. [PL] App. B "Tree-Drafting Algorithm Details"
 // (Algorithm 1) and [PL] §2 "Tree Construction and Verification"; [RB]
 // "方法步骤详情": repeatedly pop the highest-scoring expandable node, attach
@@ -249,17 +281,29 @@ int orc_topw(const float* logits, int batch, int n_depth, int vocab, int W,
 //     d+1's top-W list (rank order), shared by every depth-d node;
 //   * children are attached in rank order while fewer than B nodes exist;
 //     depth-N children are created but never pushed (not expandable);
-//   * score(child) = score(parent) + logp in binary32 (the precision the
+//   * score(child) = score(parent) + increment in binary32 (the precision the
 //     kernel ranks in), heap order = (score desc, node id asc), the root
 //     (id -1, score 0) is popped first.
-// tok/logp: [batch][n_depth][W] as produced by orc_topw.
+//
+// Scores ([PL] App. C and App. E "Drafting"; the pages give the modes and
+// the limits α -> 0 (cumulative log-prob) and α -> inf (entropy only), not
+// the formula). The increment of a child at depth d with rank r is, in
+// binary32 with H_d the entropy of depth d's draft distribution:
+//   mode 0 (cumulative log-prob): logp[d][r]
+//   mode 1 (hybrid):              logp[d][r] - (alpha * H_d)
+//   mode 2 (entropy only):        -H_d
+// so a hybrid score is cum_logp - alpha * sum_{d' <= d} H_d'.
+// tok/logp: [batch][n_depth][W] as produced by orc_topw; entropy:
+// [batch][n_depth] (unused in mode 0).
 // Outputs per sequence: parent/token/depth/score [B] (slots >= n set to
 // -1/-1/0/0), n_nodes.
 // ---------------------------------------------------------------------------
-int orc_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W, int B,
-                    int32_t* parent, int32_t* token, int32_t* depth, float* score,
-                    int32_t* n_nodes) {
+int orc_tree_expand_scored(const int32_t* tok, const float* logp, const float* entropy,
+                           int batch, int n_depth, int W, int B, int mode, float alpha,
+                           int32_t* parent, int32_t* token, int32_t* depth, float* score,
+                           int32_t* n_nodes) {
   if (batch < 0 || n_depth <= 0 || W <= 0 || B < 0) return kBadArg;
+  if (mode < 0 || mode > 2 || (mode != 0 && !entropy)) return kBadArg;
   struct Entry { float score; int32_t id; int32_t depth; };
   struct Lower {  // "a ranks below c" for std::priority_queue (max-heap)
     bool operator()(const Entry& a, const Entry& c) const {
@@ -275,6 +319,16 @@ int orc_tree_expand(const int32_t* tok, const float* logp, int batch, int n_dept
     for (int v = 0; v < B; ++v) { par[v] = -1; tk[v] = -1; dp[v] = 0; sc[v] = 0.0f; }
     const int32_t* tok_b = tok + static_cast<size_t>(b) * n_depth * W;
     const float* logp_b = logp + static_cast<size_t>(b) * n_depth * W;
+    auto increment = [&](int d, int r) -> float {   // d = 1..N
+      const float lp = logp_b[(d - 1) * W + r];
+      if (mode == 0) return lp;
+      const float h = entropy[static_cast<size_t>(b) * n_depth + d - 1];
+      if (mode == 1) {
+        const float t = alpha * h;   // one binary32 multiply
+        return lp - t;               // one binary32 subtract
+      }
+      return -h;
+    };
 
     std::priority_queue<Entry, std::vector<Entry>, Lower> heap;
     heap.push(Entry{0.0f, -1, 0});
@@ -288,13 +342,20 @@ int orc_tree_expand(const int32_t* tok, const float* logp, int batch, int n_dept
         par[v] = u.id;
         tk[v] = tok_b[(d - 1) * W + r];
         dp[v] = d;
-        sc[v] = u.score + logp_b[(d - 1) * W + r];  // one binary32 add
+        sc[v] = u.score + increment(d, r);  // one binary32 add
         if (d < n_depth) heap.push(Entry{sc[v], v, d});
       }
     }
     n_nodes[b] = count;
   }
   return 0;
+}
+
+int orc_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W, int B,
+                    int32_t* parent, int32_t* token, int32_t* depth, float* score,
+                    int32_t* n_nodes) {
+  return orc_tree_expand_scored(tok, logp, nullptr, batch, n_depth, W, B, 0, 0.0f, parent, token,
+                                depth, score, n_nodes);
 }
 
 // ---------------------------------------------------------------------------
