@@ -478,6 +478,21 @@ def main():
         g.upload()
         return g, events
 
+    def capture_fn(fn_of_step):
+        """K launches of fn_of_step(i)(), events at the two ends."""
+        events = [ctypes.c_void_p(), ctypes.c_void_p()]
+        for ev in events:
+            _ok(rt.cudaEventCreateWithFlags(ctypes.byref(ev), 0), "cudaEventCreateWithFlags")
+        g = Graph(rt, stream)
+        with torch.cuda.stream(stream):
+            with g:
+                _ok(rt.cudaEventRecordWithFlags(events[0], sptr, 1), "cudaEventRecordWithFlags")
+                for i in range(K):
+                    fn_of_step(i)()
+                _ok(rt.cudaEventRecordWithFlags(events[1], sptr, 1), "cudaEventRecordWithFlags")
+        g.upload()
+        return g, events
+
     def elapsed(events):
         ms = ctypes.c_float(0)
         _ok(rt.cudaEventElapsedTime(ctypes.byref(ms), events[0], events[1]), "cudaEventElapsedTime")
@@ -520,6 +535,76 @@ def main():
     if ex.read_error() != 0:
         raise RuntimeError("device error flag set during the timed regions")
 
+    # ---- the accepted-path K/V commit (a row beyond the step: measured alone) ----
+    # Its destinations get room for N more tokens per sequence (the workloads'
+    # caches are sized to their prefixes): a contiguous buffer, or for paged
+    # caches a small pool holding just the pages the commit writes, reached
+    # through a block table whose other entries point at page 0. The bytes
+    # moved are those of a commit into the real cache.
+    commit_sets = []
+    for i in range(R):
+        inp, bf = sets[i], bufs[i]
+        L = inp["prefix_len"].cpu()
+        if w.paged:
+            span = (w.N + 15) // 16 + 1
+            mp = (int(L.max().item()) + w.N + 15) // 16
+            table = torch.zeros((w.batch, mp), dtype=torch.int32)
+            for b_ in range(w.batch):
+                p0 = int(L[b_].item()) // 16
+                for k in range(span):
+                    if p0 + k < mp:
+                        table[b_, p0 + k] = b_ * span + k
+            kd = torch.zeros((w.batch * span, 16, w.hkv, w.D), dtype=torch.bfloat16, device=dev)
+            table = table.to(dev)
+        else:
+            table = None
+            kd = torch.zeros((w.batch, int(L.max().item()) + w.N, w.hkv, w.D),
+                             dtype=torch.bfloat16, device=dev)
+        commit_sets.append(dict(k=kd, v=torch.zeros_like(kd), table=table,
+                                new_len=torch.empty_like(inp["prefix_len"])))
+
+    def commit_fn(i):
+        inp, bf, cs = sets[i % R], bufs[i % R], commit_sets[i % R]
+        return lambda: jtree.jt_tree_commit_kv(
+            inp["k_tree"], inp["v_tree"], cs["k"], cs["v"], inp["prefix_len"], bf.acc["acc_len"],
+            bf.acc["acc_nodes"], new_prefix_len=cs["new_len"], block_table=cs["table"], exec=ex)
+
+    # Entropy scan and hybrid-scored expansion (separate outputs, so the
+    # step's own buffers are untouched).
+    ent = [torch.empty((w.batch, w.N), dtype=torch.float32, device=dev) for _ in range(R)]
+    scored = [{k: torch.empty_like(t) for k, t in bf.tree.items()} for bf in bufs]
+
+    def entropy_fn(i):
+        inp, bf = sets[i % R], bufs[i % R]
+        return lambda: jtree.jt_topw(inp["draft"], w.W, bf.tok, bf.logp, exec=ex,
+                                     entropy=ent[i % R])
+
+    def scored_fn(i):
+        bf = bufs[i % R]
+        return lambda: jtree.jt_tree_expand(bf.tok, bf.logp, w.B, out=scored[i % R], exec=ex,
+                                            entropy=ent[i % R], mode=jtree.JT_SCORE_HYBRID,
+                                            alpha=0.5)
+
+    next_ms = {}
+    with torch.cuda.stream(stream):
+        for i in range(R):
+            for fn in (commit_fn, entropy_fn, scored_fn):
+                fn(i)()
+    stream.synchronize()
+    if ex.read_error() != 0:
+        raise RuntimeError("device error flag set by a next-row call")
+    for name, fn in (("jt_tree_commit_kv", commit_fn), ("jt_topw_entropy", entropy_fn),
+                     ("jt_tree_expand_scored", scored_fn)):
+        g_c, ev_c = capture_fn(fn)
+        torch.cuda.synchronize(dev)
+        g_c.launch()
+        stream.synchronize()
+        next_ms[name] = elapsed(ev_c) / K
+        release(g_c, ev_c)
+    commit_ms = next_ms["jt_tree_commit_kv"]
+    acc_tokens_sets = [int(bf.acc["acc_len"].sum().item()) for bf in bufs]
+    commit_bytes = statistics.mean(acc_tokens_sets) * 2 * 2 * 2 * w.hkv * w.D  # K,V; read+write
+
     my_nodes = sum(nodes[i % R] for i in range(K))
     value = job_throughput(my_nodes, total_ms / 1000.0, dev)   # all ranks' nodes / slowest rank
     total_ms = max_over_ranks(total_ms, dev)
@@ -560,6 +645,21 @@ def main():
             d["tensor_frac"] = avg_work[c]["flops"] / (per_call[c] / 1e3) / (
                 peaks["bf16_tflops"] * 1e12)
         calls_out[c] = d
+
+    topw_b = avg_work["jt_topw"]["bytes"] + w.batch * w.N * 4
+    next_rows = {
+        "jt_tree_commit_kv": {
+            "us": commit_ms * 1e3, "alg_bytes": commit_bytes,
+            "hbm_frac": commit_bytes / (commit_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "note": "accepted-path K/V commit, K launches alone; not in the step"},
+        "jt_topw_entropy": {
+            "us": next_ms["jt_topw_entropy"] * 1e3, "alg_bytes": topw_b,
+            "hbm_frac": topw_b / next_ms["jt_topw_entropy"] * 1e3 / 1e9 / peaks["hbm_gbs"],
+            "note": "top-W + log-softmax + per-depth entropy in one pass; not in the step"},
+        "jt_tree_expand_scored": {
+            "us": next_ms["jt_tree_expand_scored"] * 1e3,
+            "note": "hybrid score (alpha 0.5) expansion; not in the step"},
+    }
 
     # ---- end to end through the public API with host buffers ---------------
     e2e_steps = args.e2e_steps or max(3, min(K, 200))
@@ -611,6 +711,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
                 "data": "synthetic (seeded, no dataset or weights)", "config": wdesc,
                 "impl": "libjtree", "roofline": roof, "calls": calls_out,
+                "next_rows": next_rows,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches * world,
                 "clocks": sampler.summary()}
         print(json.dumps(line), flush=True)

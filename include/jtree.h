@@ -111,6 +111,23 @@ JT_API jt_status jt_topw(const float* logits, int batch, int n_depth, int vocab,
                   int32_t* tok, float* logp, const jt_exec* exec);
 
 /* ------------------------------------------------------------------------
+ * jt_topw_entropy — jt_topw plus the entropy of each depth's draft
+ * distribution, from the same single pass over the logits.
+ * [PL] App. C "Tree-Drafting Algorithm Ablation" and App. E "Drafting": the
+ * proposer supports entropy-guided and hybrid scores built from the
+ * per-depth (marginal) entropy; jt_tree_expand_scored consumes it.
+ *
+ *   entropy fp32 [batch][n_depth]: H = -sum_j p_j ln p_j (nats) with
+ *           p = softmax(logits row); -inf logits contribute nothing; a row of
+ *           all -inf reports 0.
+ * Everything else (arguments, outputs, limits) as jt_topw. H is accumulated
+ * in fp32 (online, rescaled with the running max): |error| <= 2e-4 nats for
+ * rows of 151936 logits.
+ * ------------------------------------------------------------------------ */
+JT_API jt_status jt_topw_entropy(const float* logits, int batch, int n_depth, int vocab, int W,
+                                 int32_t* tok, float* logp, float* entropy, const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
  * jt_tree_expand — budget-B best-first tree construction.
  * [PL] App. B "Tree-Drafting Algorithm Details" (Algorithm 1) and §2 "Tree
  * Construction and Verification"; [RB] "方法步骤详情"; branch score =
@@ -135,6 +152,28 @@ JT_API jt_status jt_topw(const float* logits, int batch, int n_depth, int vocab,
 JT_API jt_status jt_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W,
                          int B, int32_t* parent, int32_t* token, int32_t* depth, float* score,
                          int32_t* n_nodes, const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
+ * jt_tree_expand_scored — jt_tree_expand with a choice of branch score.
+ * [PL] App. C "Tree-Drafting Algorithm Ablation" and App. E "Drafting":
+ * cumulative log-prob (the production default), entropy-guided and hybrid
+ * scores, the hybrid weight alpha interpolating between the two (alpha -> 0
+ * gives cumulative log-prob, alpha -> inf entropy-only). The pages give no
+ * formula; this library reads it as the child's score increment
+ *   JT_SCORE_LOGP    (0): logp[d][r]
+ *   JT_SCORE_HYBRID  (1): logp[d][r] - alpha * H_d   (binary32 multiply, then subtract)
+ *   JT_SCORE_ENTROPY (2): -H_d
+ * for a child at depth d with candidate rank r, H_d from jt_topw_entropy,
+ * so a hybrid score is cum_logp - alpha * sum of H over the path's depths.
+ * Expansion, outputs, limits and device checks as jt_tree_expand (mode 0 is
+ * exactly jt_tree_expand). entropy fp32 [batch][n_depth] may be NULL in mode 0;
+ * alpha must be finite and >= 0 in mode 1.
+ * ------------------------------------------------------------------------ */
+typedef enum { JT_SCORE_LOGP = 0, JT_SCORE_HYBRID = 1, JT_SCORE_ENTROPY = 2 } jt_score_mode;
+JT_API jt_status jt_tree_expand_scored(const int32_t* tok, const float* logp, const float* entropy,
+                                       int batch, int n_depth, int W, int B, int mode, float alpha,
+                                       int32_t* parent, int32_t* token, int32_t* depth,
+                                       float* score, int32_t* n_nodes, const jt_exec* exec);
 
 /* ------------------------------------------------------------------------
  * jt_tree_mask — tree-causal attention mask as ancestor bitmasks.

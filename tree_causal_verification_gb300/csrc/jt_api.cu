@@ -82,36 +82,72 @@ size_t jt_topw_workspace_bytes(int batch, int n_depth, int vocab, int W) {
   return 0;
 }
 
-jt_status jt_topw(const float* logits, int batch, int n_depth, int vocab, int W, int32_t* tok,
-                  float* logp, const jt_exec* exec) {
+namespace {
+
+jt_status topw_impl(const float* logits, int batch, int n_depth, int vocab, int W, int32_t* tok,
+                    float* logp, float* entropy, const jt_exec* exec) {
   if (batch < 0 || n_depth < 0 || vocab <= 0 || W < 1 || W > kMaxW || W > vocab)
     return JT_ERR_INVALID_ARG;
   if (vocab % 4 != 0) return JT_ERR_UNSUPPORTED;
   const long rows = (long)batch * n_depth;
   if (rows * 16 > 0x7FFFFFFFL) return JT_ERR_UNSUPPORTED;
   if (rows > 0 && (!logits || !tok || !logp)) return JT_ERR_INVALID_ARG;
-  if (!aligned16(logits) || !aligned16(tok) || !aligned16(logp)) return JT_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(tok) || !aligned16(logp) || !aligned16(entropy))
+    return JT_ERR_INVALID_ARG;
   Ctx c;
   jt_status st = make_ctx(exec, &c);
   if (st != JT_OK) return st;
-  return from_cuda(launch_topw(c, logits, (int)rows, vocab, W, tok, logp));
+  return from_cuda(launch_topw(c, logits, (int)rows, vocab, W, tok, logp, entropy));
 }
 
-jt_status jt_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W,
-                         int B, int32_t* parent, int32_t* token, int32_t* depth, float* score,
-                         int32_t* n_nodes, const jt_exec* exec) {
+jt_status expand_impl(const int32_t* tok, const float* logp, const float* entropy, int batch,
+                      int n_depth, int W, int B, int mode, float alpha, int32_t* parent,
+                      int32_t* token, int32_t* depth, float* score, int32_t* n_nodes,
+                      const jt_exec* exec) {
   if (batch < 0 || n_depth < 1 || n_depth > kMaxDepth || W < 1 || W > kMaxW || B < 1 || B > kMaxB)
     return JT_ERR_INVALID_ARG;
-  if (batch > 0 && (!tok || !logp || !parent || !token || !depth || !score || !n_nodes))
+  if (mode < JT_SCORE_LOGP || mode > JT_SCORE_ENTROPY) return JT_ERR_INVALID_ARG;
+  if (mode == JT_SCORE_HYBRID && !(alpha >= 0.0f && alpha <= 3.0e38f)) return JT_ERR_INVALID_ARG;
+  if (batch > 0 && (!tok || !logp || !parent || !token || !depth || !score || !n_nodes ||
+                    (mode != JT_SCORE_LOGP && !entropy)))
     return JT_ERR_INVALID_ARG;
-  const void* ptrs[] = {tok, logp, parent, token, depth, score, n_nodes};
+  const void* ptrs[] = {tok, logp, entropy, parent, token, depth, score, n_nodes};
   for (const void* p : ptrs)
     if (!aligned16(p)) return JT_ERR_INVALID_ARG;
   Ctx c;
   jt_status st = make_ctx(exec, &c);
   if (st != JT_OK) return st;
-  return from_cuda(launch_tree_expand(c, tok, logp, batch, n_depth, W, B, parent, token, depth,
+  return from_cuda(launch_tree_expand(c, tok, logp, mode == JT_SCORE_LOGP ? nullptr : entropy,
+                                      mode, alpha, batch, n_depth, W, B, parent, token, depth,
                                       score, n_nodes));
+}
+
+}  // namespace
+
+jt_status jt_topw(const float* logits, int batch, int n_depth, int vocab, int W, int32_t* tok,
+                  float* logp, const jt_exec* exec) {
+  return topw_impl(logits, batch, n_depth, vocab, W, tok, logp, nullptr, exec);
+}
+
+jt_status jt_topw_entropy(const float* logits, int batch, int n_depth, int vocab, int W,
+                          int32_t* tok, float* logp, float* entropy, const jt_exec* exec) {
+  if ((long)batch * n_depth > 0 && !entropy) return JT_ERR_INVALID_ARG;
+  return topw_impl(logits, batch, n_depth, vocab, W, tok, logp, entropy, exec);
+}
+
+jt_status jt_tree_expand(const int32_t* tok, const float* logp, int batch, int n_depth, int W,
+                         int B, int32_t* parent, int32_t* token, int32_t* depth, float* score,
+                         int32_t* n_nodes, const jt_exec* exec) {
+  return expand_impl(tok, logp, nullptr, batch, n_depth, W, B, JT_SCORE_LOGP, 0.0f, parent, token,
+                     depth, score, n_nodes, exec);
+}
+
+jt_status jt_tree_expand_scored(const int32_t* tok, const float* logp, const float* entropy,
+                                int batch, int n_depth, int W, int B, int mode, float alpha,
+                                int32_t* parent, int32_t* token, int32_t* depth, float* score,
+                                int32_t* n_nodes, const jt_exec* exec) {
+  return expand_impl(tok, logp, entropy, batch, n_depth, W, B, mode, alpha, parent, token, depth,
+                     score, n_nodes, exec);
 }
 
 jt_status jt_tree_mask(const int32_t* parent, const int32_t* n_nodes, int batch, int B,

@@ -19,6 +19,12 @@
 // definition. The sequence's N x W candidates are staged in shared memory
 // first, so no pop waits on a global load (the depth that selects the next
 // candidate row is only known once the pop is done).
+//
+// Score modes (paperlayer.ai App. C "Tree-Drafting Algorithm Ablation" and
+// App. E "Drafting": cumulative log-prob, entropy-guided and hybrid scores).
+// A child at depth d with rank r adds, in binary32, logp[d][r] (mode 0),
+// logp[d][r] - alpha * H_d (mode 1, one multiply and one subtract), or -H_d
+// (mode 2). The increments are formed once while staging.
 #include <climits>
 
 #include "jt_internal.cuh"
@@ -30,13 +36,14 @@ constexpr int kWarpsPerBlock = 4;
 
 template <int SLOTS>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ logp, int batch,
+tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ logp,
+                   const float* __restrict__ entropy, int mode, float alpha, int batch,
                    int N, int W, int B, int32_t* __restrict__ parent_o,
                    int32_t* __restrict__ token_o, int32_t* __restrict__ depth_o,
                    float* __restrict__ score_o, int32_t* __restrict__ n_nodes_o) {
   __shared__ float score_s[kWarpsPerBlock][kMaxB];
   __shared__ uint8_t depth_s[kWarpsPerBlock][kMaxB];
-  extern __shared__ int32_t cand_s[];   // per warp: N*W tokens then N*W log-probs
+  extern __shared__ int32_t cand_s[];   // per warp: N*W tokens then N*W score increments
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -49,7 +56,13 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
   float* lp = reinterpret_cast<float*>(tk + nw);
   for (int i = lane; i < nw; i += 32) {
     tk[i] = __ldg(tok + (size_t)b * nw + i);
-    lp[i] = __ldg(logp + (size_t)b * nw + i);
+    const float l = __ldg(logp + (size_t)b * nw + i);
+    float inc = l;
+    if (mode != 0) {
+      const float h = __ldg(entropy + (size_t)b * N + i / W);
+      inc = mode == 1 ? __fsub_rn(l, __fmul_rn(alpha, h)) : -h;
+    }
+    lp[i] = inc;
   }
   __syncwarp();
   int32_t* par = parent_o + (size_t)b * B;
@@ -135,7 +148,8 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
 
 }  // namespace
 
-cudaError_t launch_tree_expand(const Ctx& c, const int32_t* tok, const float* logp, int batch,
+cudaError_t launch_tree_expand(const Ctx& c, const int32_t* tok, const float* logp,
+                               const float* entropy, int mode, float alpha, int batch,
                                int n_depth, int W, int B, int32_t* parent, int32_t* token,
                                int32_t* depth, float* score, int32_t* n_nodes) {
   if (batch == 0) return cudaSuccess;
@@ -148,8 +162,8 @@ cudaError_t launch_tree_expand(const Ctx& c, const int32_t* tok, const float* lo
             : slots <= 2 ? tree_expand_kernel<2>
             : slots <= 4 ? tree_expand_kernel<4>
                          : tree_expand_kernel<8>;
-  return launch_kernel(kern, grid, block, smem, c.stream, 1, tok, logp, batch, n_depth, W, B,
-                       parent, token, depth, score, n_nodes);
+  return launch_kernel(kern, grid, block, smem, c.stream, 1, tok, logp, entropy, mode, alpha,
+                       batch, n_depth, W, B, parent, token, depth, score, n_nodes);
 }
 
 }  // namespace jt

@@ -77,11 +77,12 @@ int device_sm_count(int device);
 // return the cudaError_t of the launch.
 cudaError_t launch_tree_mask(const Ctx&, const int32_t* parent, const int32_t* n_nodes, int batch,
                              int B, uint32_t* mask);
-cudaError_t launch_tree_expand(const Ctx&, const int32_t* tok, const float* logp, int batch,
+cudaError_t launch_tree_expand(const Ctx&, const int32_t* tok, const float* logp,
+                               const float* entropy, int mode, float alpha, int batch,
                                int n_depth, int W, int B, int32_t* parent, int32_t* token,
                                int32_t* depth, float* score, int32_t* n_nodes);
 cudaError_t launch_topw(const Ctx&, const float* logits, int rows, int vocab, int W, int32_t* tok,
-                        float* logp);
+                        float* logp, float* entropy);
 size_t accept_workspace_bytes(int batch, int B, int n_depth, int vocab);
 cudaError_t launch_tree_accept(const Ctx&, const float* target, const int32_t* parent,
                                const int32_t* token, const int32_t* n_nodes, int batch, int B,

@@ -6,7 +6,8 @@
 // 128-bit non-allocating loads, two batches of float4s per thread in flight.
 // Per thread: a sorted top-K list in registers, guarded by a one-compare
 // rejection test of each float4's maximum against the current K-th value,
-// and an online log-sum-exp in the log2 domain.
+// and an online log-sum-exp in the log2 domain (optionally with the sum that
+// gives the distribution's entropy).
 //
 // Selection (warp, then block, then cluster) runs K rounds of a warp-wide
 // argmax: every lane offers its best remaining candidate; __reduce_max_sync
@@ -73,24 +74,57 @@ struct TopK {
   }
 };
 
-// Online log-sum-exp in log2 units: the row's running max m (of x*log2e)
-// and s = sum 2^(x*log2e - m).
+// Online log-sum-exp in log2 units: with u = x*log2e, the row's running max
+// m of u, s = sum 2^(u - m) and (entropy scans only) t = sum (u - m) 2^(u - m).
+// Then ln Z = m ln2 + ln s and the entropy of softmax(x) is ln s - ln2 * t/s
+// nats. When m grows by -d (d = m_old - m_new < 0), s' = s 2^d and
+// t' = (t + d s) 2^d.
 struct Lse {
-  float m, s;
-  __device__ __forceinline__ void init() { m = -INFINITY; s = 0.0f; }
-  __device__ __forceinline__ void combine(float m2, float s2) {
+  float m, s, t;
+  __device__ __forceinline__ void init() { m = -INFINITY; s = 0.0f; t = 0.0f; }
+  __device__ __forceinline__ void combine(float m2, float s2, float t2) {
     if (m2 == -INFINITY) return;
-    if (m == -INFINITY) { m = m2; s = s2; return; }
-    if (m2 > m) { s = s * fast_ex2(m - m2) + s2; m = m2; }
-    else { s = s + s2 * fast_ex2(m2 - m); }
+    if (m == -INFINITY) { m = m2; s = s2; t = t2; return; }
+    if (m2 > m) {
+      const float d = m - m2, f = fast_ex2(d);
+      t = fmaf(fmaf(d, s, t), f, t2);
+      s = fmaf(s, f, s2);
+      m = m2;
+    } else {
+      const float d = m2 - m, f = fast_ex2(d);
+      t = fmaf(fmaf(d, s2, t2), f, t);
+      s = fmaf(s2, f, s);
+    }
   }
   __device__ __forceinline__ void warp_reduce() {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
       const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, off);
-      combine(m2, s2);
+      const float t2 = __shfl_xor_sync(0xFFFFFFFFu, t, off);
+      combine(m2, s2, t2);
     }
+  }
+  // Raises the running max to bm (> m), rescaling s (and t when ENT).
+  template <bool ENT>
+  __device__ __forceinline__ void raise(float bm) {
+    if (m == -INFINITY) {
+      s = 0.0f;
+      t = 0.0f;
+    } else {
+      const float d = m - bm, f = fast_ex2(d);
+      if (ENT) t = fmaf(d, s, t) * f;
+      s *= f;
+    }
+    m = bm;
+  }
+  // Adds one element with u - m = a (a <= 0; -inf for a -inf logit).
+  template <bool ENT>
+  __device__ __forceinline__ float term(float a, float& tacc) const {
+    const float e = fast_ex2(a);
+    // a = -inf (or below the flush range) gives e = 0: the clamp keeps 0 * a finite.
+    if (ENT) tacc = fmaf(fmaxf(a, -126.0f), e, tacc);
+    return e;
   }
 };
 
@@ -107,7 +141,7 @@ template <int K>
 struct ScanPartial {
   float v[K];
   int i[K];
-  float m, s;
+  float m, s, t;
 };
 
 // K rounds of warp-wide argmax. Lane l offers the sorted list (cv, ci) of
@@ -151,7 +185,7 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 // refresh: every lane of the warp processes a batch in this call and the
 // warp-wide pruning bound is recomputed afterwards (K rounds of warp argmax,
 // so it is done only while the bound is still tightening quickly).
-template <int K, bool LSE>
+template <int K, bool LSE, bool ENT>
 __device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0, TopK<K>& top,
                                            Lse& lse, bool refresh) {
   float mx[kScanBatch];
@@ -160,19 +194,19 @@ __device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0
     mx[u] = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
   if (LSE) {
     const float bm2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * kLog2e;
-    if (bm2 > lse.m) {
-      lse.s = (lse.m == -INFINITY) ? 0.0f : lse.s * fast_ex2(lse.m - bm2);
-      lse.m = bm2;
-    }
+    if (bm2 > lse.m) lse.raise<ENT>(bm2);
     if (lse.m != -INFINITY) {
       const float nm = -lse.m;
-      float a0 = 0.0f, a1 = 0.0f;
+      float a0 = 0.0f, a1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) {
-        a0 += fast_ex2(fmaf(x[u].x, kLog2e, nm)) + fast_ex2(fmaf(x[u].y, kLog2e, nm));
-        a1 += fast_ex2(fmaf(x[u].z, kLog2e, nm)) + fast_ex2(fmaf(x[u].w, kLog2e, nm));
+        a0 += lse.term<ENT>(fmaf(x[u].x, kLog2e, nm), t0) +
+              lse.term<ENT>(fmaf(x[u].y, kLog2e, nm), t1);
+        a1 += lse.term<ENT>(fmaf(x[u].z, kLog2e, nm), t0) +
+              lse.term<ENT>(fmaf(x[u].w, kLog2e, nm), t1);
       }
       lse.s += a0 + a1;
+      if (ENT) lse.t += t0 + t1;
     }
   }
 #pragma unroll
@@ -198,7 +232,7 @@ __device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0
 // Streams float4s [lo4, hi4) of `row` into per-thread state: full batches
 // without bounds checks, ping-ponging two register buffers so that one batch
 // is in flight while the other is processed, then a checked tail.
-template <int K, bool LSE>
+template <int K, bool LSE, bool ENT = false>
 __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int lo4, int hi4,
                                              TopK<K>& top, Lse& lse) {
   const float4* r4 = reinterpret_cast<const float4*>(row);
@@ -221,7 +255,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) b[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
     }
-    scan_batch<K, LSE>(a, base + tid, top, lse, refresh());
+    scan_batch<K, LSE, ENT>(a, base + tid, top, lse, refresh());
     base += STEP;
     if (!nb) break;
     const bool na = base + STEP < full_end;
@@ -229,7 +263,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) a[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
     }
-    scan_batch<K, LSE>(b, base + tid, top, lse, refresh());
+    scan_batch<K, LSE, ENT>(b, base + tid, top, lse, refresh());
     base += STEP;
     if (!na) break;
   }
@@ -254,7 +288,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
         cnt += j < hi4;
       }
       if (cnt == kScanBatch) {
-        scan_batch<K, LSE>(x, full_end + tid, top, lse, false);
+        scan_batch<K, LSE, ENT>(x, full_end + tid, top, lse, false);
       } else {
         // Partial batch: element-wise, in index order.
         if (LSE) {
@@ -263,18 +297,19 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
           for (int u = 0; u < kScanBatch; ++u)
             if (u < cnt) bm = fmaxf(bm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
           const float bm2 = bm * kLog2e;
-          if (bm2 > lse.m) {
-            lse.s = (lse.m == -INFINITY) ? 0.0f : lse.s * fast_ex2(lse.m - bm2);
-            lse.m = bm2;
-          }
+          if (bm2 > lse.m) lse.raise<ENT>(bm2);
           if (lse.m != -INFINITY) {
-            float acc = 0.0f;
+            const float nm = -lse.m;
+            float acc = 0.0f, tacc = 0.0f;
 #pragma unroll
             for (int u = 0; u < kScanBatch; ++u)
               if (u < cnt)
-                acc += fast_ex2(fmaf(x[u].x, kLog2e, -lse.m)) + fast_ex2(fmaf(x[u].y, kLog2e, -lse.m)) +
-                       fast_ex2(fmaf(x[u].z, kLog2e, -lse.m)) + fast_ex2(fmaf(x[u].w, kLog2e, -lse.m));
+                acc += lse.term<ENT>(fmaf(x[u].x, kLog2e, nm), tacc) +
+                       lse.term<ENT>(fmaf(x[u].y, kLog2e, nm), tacc) +
+                       lse.term<ENT>(fmaf(x[u].z, kLog2e, nm), tacc) +
+                       lse.term<ENT>(fmaf(x[u].w, kLog2e, nm), tacc);
             lse.s += acc;
+            if (ENT) lse.t += tacc;
           }
         }
 #pragma unroll
@@ -307,6 +342,7 @@ __device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial
     for (int k = 0; k < K; ++k) { warp_parts[warp].v[k] = wv[k]; warp_parts[warp].i[k] = wi[k]; }
     warp_parts[warp].m = lse.m;
     warp_parts[warp].s = lse.s;
+    warp_parts[warp].t = lse.t;
   }
   __syncthreads();
   if (warp == 0) {
@@ -321,6 +357,7 @@ __device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial
       len = K;
       l.m = warp_parts[lane].m;
       l.s = warp_parts[lane].s;
+      l.t = warp_parts[lane].t;
     } else {
 #pragma unroll
       for (int k = 0; k < K; ++k) { cv[k] = -INFINITY; ci[k] = INT_MAX; }
@@ -339,6 +376,7 @@ __device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial
       for (int k = 0; k < K; ++k) { out->v[k] = bv[k]; out->i[k] = bi[k]; }
       out->m = l.m;
       out->s = l.s;
+      out->t = l.t;
     }
   }
   __syncthreads();
@@ -356,6 +394,7 @@ __device__ __forceinline__ bool cluster_reduce(ScanPartial<K>* mine, int S, TopK
     for (int k = 0; k < K; ++k) { top.v[k] = mine->v[k]; top.i[k] = mine->i[k]; }
     lse.m = mine->m;
     lse.s = mine->s;
+    lse.t = mine->t;
     return true;
   }
   cg::cluster_group cluster = cg::this_cluster();
@@ -373,6 +412,7 @@ __device__ __forceinline__ bool cluster_reduce(ScanPartial<K>* mine, int S, TopK
       len = K;
       lse.m = p->m;
       lse.s = p->s;
+      lse.t = p->t;
     } else {
 #pragma unroll
       for (int k = 0; k < K; ++k) { cv[k] = -INFINITY; ci[k] = INT_MAX; }

@@ -7,7 +7,10 @@
 // the full vocabulary; ranking (x desc, token id asc).
 //
 // The row is read exactly once: the top-W selection and the log-sum-exp run
-// in the same pass (jt_rowscan.cuh). Rows are split over a thread-block
+// in the same pass (jt_rowscan.cuh), and so does the entropy of the depth's
+// draft distribution when it is asked for (entropy-guided and hybrid tree
+// scores, paperlayer.ai App. C "Tree-Drafting Algorithm Ablation" and App. E
+// "Drafting"): H = ln s - ln2 * t / s from the same online sums. Rows are split over a thread-block
 // cluster when there are too few rows to fill the GPU (batch 1: 16 rows of
 // 151936 logits -> 16-CTA clusters), and the cluster merges its partials in
 // distributed shared memory.
@@ -16,10 +19,10 @@
 namespace jt {
 namespace {
 
-template <int K>
+template <int K, bool ENT>
 __global__ void __launch_bounds__(kScanThreads)
 topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __restrict__ tok,
-            float* __restrict__ logp) {
+            float* __restrict__ logp, float* __restrict__ entropy) {
   __shared__ ScanPartial<K> warp_parts[kScanWarps];
   __shared__ ScanPartial<K> part;
   const int row = blockIdx.x / S;
@@ -32,12 +35,13 @@ topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __re
   Lse lse;
   lse.init();
   grid_dependency_sync();
-  scan_segment<K, true>(logits + (size_t)row * V, lo, hi, top, lse);
+  scan_segment<K, true, ENT>(logits + (size_t)row * V, lo, hi, top, lse);
   block_reduce<K, true>(top, lse, &part, warp_parts);
   if (cluster_reduce<K, true>(&part, S, top, lse)) {
     // lse.m is the max of x*log2(e) and lse.s = sum 2^(x*log2(e) - m), so
     // ln Z = m * ln 2 + ln s.
-    const float lnZ = fmaf(lse.m, 0.6931471805599453f, logf(lse.s));
+    const float ln_s = logf(lse.s);
+    const float lnZ = fmaf(lse.m, 0.6931471805599453f, ln_s);
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       if (k < W) {
@@ -45,27 +49,33 @@ topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __re
         logp[(size_t)row * W + k] = top.v[k] - lnZ;
       }
     }
+    if (ENT)
+      entropy[row] = lse.s > 0.0f ? fmaf(-0.6931471805599453f, lse.t / lse.s, ln_s) : 0.0f;
   }
 }
 
 template <int K>
 cudaError_t launch_k(const Ctx& c, const float* logits, int rows, int V, int W, int32_t* tok,
-                     float* logp) {
+                     float* logp, float* entropy) {
   const int S = pick_row_split(rows, V / 4, c.num_sms, 16);
-  return launch_clustered(topw_kernel<K>, rows * S, S, c.stream, logits, V, W, S, tok, logp);
+  if (entropy)
+    return launch_clustered(topw_kernel<K, true>, rows * S, S, c.stream, logits, V, W, S, tok,
+                            logp, entropy);
+  return launch_clustered(topw_kernel<K, false>, rows * S, S, c.stream, logits, V, W, S, tok, logp,
+                          entropy);
 }
 
 }  // namespace
 
 cudaError_t launch_topw(const Ctx& c, const float* logits, int rows, int V, int W, int32_t* tok,
-                        float* logp) {
+                        float* logp, float* entropy) {
   if (rows == 0) return cudaSuccess;
-  if (W <= 1) return launch_k<1>(c, logits, rows, V, W, tok, logp);
-  if (W <= 2) return launch_k<2>(c, logits, rows, V, W, tok, logp);
-  if (W <= 4) return launch_k<4>(c, logits, rows, V, W, tok, logp);
-  if (W <= 8) return launch_k<8>(c, logits, rows, V, W, tok, logp);
-  if (W <= 16) return launch_k<16>(c, logits, rows, V, W, tok, logp);
-  return launch_k<32>(c, logits, rows, V, W, tok, logp);
+  if (W <= 1) return launch_k<1>(c, logits, rows, V, W, tok, logp, entropy);
+  if (W <= 2) return launch_k<2>(c, logits, rows, V, W, tok, logp, entropy);
+  if (W <= 4) return launch_k<4>(c, logits, rows, V, W, tok, logp, entropy);
+  if (W <= 8) return launch_k<8>(c, logits, rows, V, W, tok, logp, entropy);
+  if (W <= 16) return launch_k<16>(c, logits, rows, V, W, tok, logp, entropy);
+  return launch_k<32>(c, logits, rows, V, W, tok, logp, entropy);
 }
 
 }  // namespace jt

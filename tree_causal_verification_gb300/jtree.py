@@ -34,7 +34,8 @@ STATUS_NAMES = {0: "JT_OK", 1: "JT_ERR_INVALID_ARG", 2: "JT_ERR_UNSUPPORTED", 3:
 EXPORTED = ["jt_status_str", "jt_read_device_error", "jt_topw_workspace_bytes", "jt_topw",
             "jt_tree_expand", "jt_tree_mask", "jt_tree_attn_workspace_bytes", "jt_tree_attn",
             "jt_tree_accept_workspace_bytes", "jt_tree_accept", "jt_tree_accept_noalloc",
-            "jt_tree_commit_kv"]
+            "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored"]
+JT_SCORE_LOGP, JT_SCORE_HYBRID, JT_SCORE_ENTROPY = 0, 1, 2
 
 
 class JtError(RuntimeError):
@@ -96,6 +97,11 @@ def load(path: str = LIB_PATH):
             lib.jt_tree_expand.argtypes = [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                                            _vp, _vp, _vp, _pexec]
             lib.jt_tree_mask.argtypes = [_vp, _vp, _c_int, _c_int, _vp, _pexec]
+            lib.jt_topw_entropy.argtypes = [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
+                                            _pexec]
+            lib.jt_tree_expand_scored.argtypes = [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                                  _c_int, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
+                                                  _pexec]
             lib.jt_tree_attn_workspace_bytes.restype = _c_size
             lib.jt_tree_attn_workspace_bytes.argtypes = [ctypes.POINTER(jt_attn_args)]
             lib.jt_tree_attn.argtypes = [ctypes.POINTER(jt_attn_args), _pexec]
@@ -107,7 +113,7 @@ def load(path: str = LIB_PATH):
             lib.jt_tree_commit_kv.argtypes = [ctypes.POINTER(jt_commit_args), _pexec]
             for name in ("jt_read_device_error", "jt_topw", "jt_tree_expand", "jt_tree_mask",
                          "jt_tree_attn", "jt_tree_accept", "jt_tree_accept_noalloc",
-                         "jt_tree_commit_kv"):
+                         "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored"):
                 getattr(lib, name).restype = _c_int
             _lib = lib
     return _lib
@@ -185,8 +191,11 @@ def _exec(ex):
     return _default_execs[dev]
 
 
-def jt_topw(logits, W, tok=None, logp=None, exec=None):
-    """Top-W tokens and log-probs per row: logits fp32 [batch][N][V]."""
+def jt_topw(logits, W, tok=None, logp=None, exec=None, entropy=None, with_entropy=False):
+    """Top-W tokens and log-probs per row: logits fp32 [batch][N][V].
+
+    with_entropy (or an entropy buffer) also returns the per-row entropy
+    fp32 [batch][N] (jt_topw_entropy)."""
     batch, N, V = logits.shape
     dev = logits.device
     tok = torch.empty((batch, N, W), dtype=torch.int32, device=dev) if tok is None else tok
@@ -197,13 +206,24 @@ def jt_topw(logits, W, tok=None, logp=None, exec=None):
     lib = load()
     ex = _exec(exec).reserve(lib.jt_topw_workspace_bytes(batch, N, V, W))
     c = ex.c()
-    _check(lib.jt_topw(_ptr(logits), batch, N, V, W, _ptr(tok), _ptr(logp), ctypes.byref(c)),
-           "jt_topw")
-    return tok, logp
+    if entropy is None and not with_entropy:
+        _check(lib.jt_topw(_ptr(logits), batch, N, V, W, _ptr(tok), _ptr(logp), ctypes.byref(c)),
+               "jt_topw")
+        return tok, logp
+    if entropy is None:
+        entropy = torch.empty((batch, N), dtype=torch.float32, device=dev)
+    _need(entropy, torch.float32, (batch, N), "entropy")
+    _check(lib.jt_topw_entropy(_ptr(logits), batch, N, V, W, _ptr(tok), _ptr(logp),
+                               _ptr(entropy), ctypes.byref(c)), "jt_topw_entropy")
+    return tok, logp, entropy
 
 
-def jt_tree_expand(tok, logp, B, out=None, exec=None):
-    """Best-first expansion; returns dict(parent, token, depth, score, n_nodes)."""
+def jt_tree_expand(tok, logp, B, out=None, exec=None, entropy=None, mode=JT_SCORE_LOGP,
+                   alpha=0.0):
+    """Best-first expansion; returns dict(parent, token, depth, score, n_nodes).
+
+    mode / entropy / alpha select the branch score (jt_tree_expand_scored):
+    0 cumulative log-prob, 1 hybrid logp - alpha*H_d, 2 entropy only -H_d."""
     batch, N, W = tok.shape
     dev = tok.device
     if out is None:
@@ -219,9 +239,17 @@ def jt_tree_expand(tok, logp, B, out=None, exec=None):
     _need(out["score"], torch.float32, (batch, B), "score")
     _need(out["n_nodes"], torch.int32, (batch,), "n_nodes")
     c = _exec(exec).c()
-    _check(load().jt_tree_expand(_ptr(tok), _ptr(logp), batch, N, W, B, _ptr(out["parent"]),
-                                 _ptr(out["token"]), _ptr(out["depth"]), _ptr(out["score"]),
-                                 _ptr(out["n_nodes"]), ctypes.byref(c)), "jt_tree_expand")
+    outs = (_ptr(out["parent"]), _ptr(out["token"]), _ptr(out["depth"]), _ptr(out["score"]),
+            _ptr(out["n_nodes"]))
+    if mode == JT_SCORE_LOGP and entropy is None:
+        _check(load().jt_tree_expand(_ptr(tok), _ptr(logp), batch, N, W, B, *outs,
+                                     ctypes.byref(c)), "jt_tree_expand")
+        return out
+    if entropy is not None:
+        _need(entropy, torch.float32, (batch, N), "entropy")
+    _check(load().jt_tree_expand_scored(_ptr(tok), _ptr(logp), _ptr(entropy), batch, N, W, B,
+                                        int(mode), float(alpha), *outs, ctypes.byref(c)),
+           "jt_tree_expand_scored")
     return out
 
 
