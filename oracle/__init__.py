@@ -27,6 +27,7 @@ _u32p = ctypes.POINTER(ctypes.c_uint32)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_u64p = ctypes.POINTER(ctypes.c_uint64)
 
 
 def build(force: bool = False) -> str:
@@ -59,6 +60,12 @@ def _load():
             lib.orc_tree_accept.argtypes = [_f32p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_int, _i32p, _i32p, _i32p, _i32p]
             lib.orc_row_entropy.argtypes = [_f32p, ctypes.c_long, ctypes.c_int, _f32p]
+            lib.orc_tree_accept_sampled.argtypes = [
+                _f32p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_float, ctypes.c_uint64, _i32p, _i32p, _i32p, _i32p]
+            lib.orc_series_ln.argtypes = [_f32p, ctypes.c_long, _f32p]
+            lib.orc_splitmix64.argtypes = [ctypes.c_uint64, _u64p, ctypes.c_long, _u64p]
+            lib.orc_gumbel.argtypes = [ctypes.c_uint64, _u64p, ctypes.c_long, _f32p]
             lib.orc_tree_expand_scored.argtypes = [
                 _i32p, _f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_float, _i32p, _i32p, _i32p, _f32p, _i32p]
@@ -68,7 +75,7 @@ def _load():
                 ctypes.c_int, _i32p, _i32p, _i32p, _i32p]
             for f in (lib.orc_tree_mask, lib.orc_tree_attn, lib.orc_topw, lib.orc_tree_expand,
                       lib.orc_tree_accept, lib.orc_tree_commit_kv, lib.orc_row_entropy,
-                      lib.orc_tree_expand_scored):
+                      lib.orc_tree_expand_scored, lib.orc_tree_accept_sampled):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -218,6 +225,52 @@ def tree_accept(target, parent, token, n_nodes, n_depth):
                                    _ptr(acc_nodes, _i32p), _ptr(bonus, _i32p)),
            "orc_tree_accept")
     return dict(acc_len=acc_len, acc_tokens=acc_tokens, acc_nodes=acc_nodes, bonus=bonus)
+
+
+def tree_accept_sampled(target, parent, token, n_nodes, n_depth, temperature, seed):
+    """Temperature-T acceptance (one Gumbel-max target draw per visited node)
+    -> dict(acc_len, acc_tokens, acc_nodes, bonus). The binary32 reciprocal
+    of the temperature is what both sides multiply by."""
+    target = _arr(target, np.float32)
+    parent = _arr(parent, np.int32)
+    token = _arr(token, np.int32)
+    n_nodes = _arr(n_nodes, np.int32)
+    batch, B = parent.shape
+    vocab = target.shape[-1]
+    assert target.shape == (batch, B + 1, vocab)
+    inv_t = float(np.float32(1.0) / np.float32(temperature))
+    acc_len = np.zeros((batch,), np.int32)
+    acc_tokens = np.zeros((batch, n_depth), np.int32)
+    acc_nodes = np.zeros((batch, n_depth), np.int32)
+    bonus = np.zeros((batch,), np.int32)
+    _check(_load().orc_tree_accept_sampled(_ptr(target, _f32p), _ptr(parent, _i32p),
+                                           _ptr(token, _i32p), _ptr(n_nodes, _i32p), batch, B,
+                                           n_depth, vocab, inv_t, int(seed) & (2 ** 64 - 1),
+                                           _ptr(acc_len, _i32p), _ptr(acc_tokens, _i32p),
+                                           _ptr(acc_nodes, _i32p), _ptr(bonus, _i32p)),
+           "orc_tree_accept_sampled")
+    return dict(acc_len=acc_len, acc_tokens=acc_tokens, acc_nodes=acc_nodes, bonus=bonus)
+
+
+def series_ln(x):
+    x = _arr(x, np.float32)
+    out = np.zeros_like(x)
+    _load().orc_series_ln(_ptr(x, _f32p), x.size, _ptr(out, _f32p))
+    return out
+
+
+def splitmix64(seed, k):
+    k = _arr(k, np.uint64)
+    out = np.zeros_like(k)
+    _load().orc_splitmix64(int(seed) & (2 ** 64 - 1), _ptr(k, _u64p), k.size, _ptr(out, _u64p))
+    return out
+
+
+def gumbel(seed, k):
+    k = _arr(k, np.uint64)
+    out = np.zeros(k.shape, np.float32)
+    _load().orc_gumbel(int(seed) & (2 ** 64 - 1), _ptr(k, _u64p), k.size, _ptr(out, _f32p))
+    return out
 
 
 def tree_commit_kv(k_tree, v_tree, k_cache, v_cache, prefix_len, acc_len, acc_nodes,

@@ -16,6 +16,7 @@
 //                      (orc_tree_expand_scored: hybrid / entropy-only scores)
 //   orc_tree_accept  - sequential argmax + walk down the tree
 //   orc_tree_commit_kv - append the accepted path's K/V rows to the prefix cache
+//   orc_tree_accept_sampled - temperature-T acceptance, one target draw per node
 //
 // Sources (page title, site, section):
 //   [PL]  "JetSpec: Breaking the Scaling Ceiling of Speculative Decoding with
@@ -42,6 +43,50 @@ namespace {
 constexpr int kBadArg = -1;
 constexpr int kBadTree = -2;
 constexpr int kBadToken = -3;
+
+// SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+// generators", OOPSLA 2014): the state advances by the golden-ratio gamma and
+// each output is the state passed through the 64-bit finaliser. Output k
+// (k = 1, 2, ...) of the generator seeded with s is mix64(s + k * gamma), so
+// any output can be computed directly from its index.
+uint64_t splitmix64_output(uint64_t seed, uint64_t k) {
+  uint64_t z = seed + k * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Natural log of a positive normal binary32 from ln(m 2^e) = e ln2 +
+// 2 atanh(f), f = (m-1)/(m+1), m in [sqrt(1/2), sqrt(2)), with the atanh
+// series f + f^3/3 + ... + f^9/9 (|f| <= 0.172, truncation < 1e-8 relative).
+// Every step is one binary32 operation (fused multiply-adds where written),
+// so any implementation that takes the same steps gets the same bits.
+float series_ln(float x) {
+  uint32_t u;
+  std::memcpy(&u, &x, sizeof u);
+  int e = static_cast<int>(u >> 23) - 127;
+  const uint32_t mb = (u & 0x7FFFFFu) | 0x3F800000u;
+  float m;
+  std::memcpy(&m, &mb, sizeof m);
+  if (m > 1.41421356f) { m = m * 0.5f; e += 1; }
+  const float f = (m - 1.0f) / (m + 1.0f);
+  const float f2 = f * f;
+  float p = std::fma(f2, 1.0f / 9.0f, 1.0f / 7.0f);
+  p = std::fma(p, f2, 0.2f);
+  p = std::fma(p, f2, 1.0f / 3.0f);
+  p = std::fma(p, f2, 1.0f);
+  const float lm = (2.0f * f) * p;
+  return std::fma(static_cast<float>(e), 0.693147182f, lm);
+}
+
+// Gumbel(0,1) noise for draw index k of the stream `seed`: U from the top 23
+// bits of the k-th SplitMix64 output, U = (bits + 1/2) 2^-23 in (0, 1), and
+// G = -ln(-ln U) with series_ln.
+float gumbel_noise(uint64_t seed, uint64_t k) {
+  const uint64_t h = splitmix64_output(seed, k);
+  const float u = (static_cast<float>(static_cast<uint32_t>(h >> 41)) + 0.5f) * 1.1920928955078125e-7f;
+  return -series_ln(-series_ln(u));
+}
 
 double widen_bf16(uint16_t bits) {
   // A bf16 value is the top half of an IEEE binary32; widening is exact.
@@ -482,6 +527,90 @@ int orc_tree_commit_kv(int batch, int B, int n_depth, int hkv, int D,
     new_prefix_len[b] = L + a;
   }
   return rc;
+}
+
+// ---------------------------------------------------------------------------
+// Temperature-T tree acceptance. [PP] App. F.3 "Lossless verification": every
+// committed token is the target's own draw at any temperature; for a draft
+// fixed before verification each draft token is checked with a point-mass
+// proposal and accepted with the target probability. [PP] App. F.1: for a
+// chain this gives P(accept d1, reject d2, draw b) = p(d1) (1 - p(d2|d1))
+// p(b|d1) / (1 - p(d2|d1)) = p(d1) p(b|d1) (the 0.24 worked example).
+//
+// Reading for trees (the pages treat chains): at the current node draw one
+// token y from softmax(target row / T); if a child carries y, accept it and
+// continue from it, else y is the bonus token and the walk ends. For a chain
+// this is exactly the point-mass rule above; for several children it is the
+// same rule applied to the children in turn (each rejection removes that
+// child's token from the residual), which again commits a draw of the target.
+//
+// The draw uses the Gumbel-max form: y = argmax_j (x_j / T + G_j), lowest j on
+// ties, with G_j = gumbel_noise(seed, k) for draw index
+//   k = ((b * (B+1) + r) << 32 | j) + 1      (r = 0 for the root row, 1+v
+//                                            for node v's row)
+// computed in binary32: t = x_j * (1/T) (one multiply by the binary32
+// reciprocal inv_T the caller passes), key = t + G_j (one add).
+// Everything else (layouts, validation, outputs) as orc_tree_accept.
+// ---------------------------------------------------------------------------
+int orc_tree_accept_sampled(const float* target, const int32_t* parent, const int32_t* token,
+                            const int32_t* n_nodes, int batch, int B, int n_depth, int vocab,
+                            float inv_T, uint64_t seed, int32_t* acc_len, int32_t* acc_tokens,
+                            int32_t* acc_nodes, int32_t* bonus) {
+  if (batch < 0 || B < 0 || n_depth <= 0 || vocab <= 0 || !(inv_T > 0.0f)) return kBadArg;
+  auto draw = [&](int b, int r, const float* row) {
+    const uint64_t base = (static_cast<uint64_t>(b) * (B + 1) + r) << 32;
+    int best = -1;
+    float bk = 0.0f;
+    for (int j = 0; j < vocab; ++j) {
+      if (row[j] == -std::numeric_limits<float>::infinity()) continue;
+      const float t = row[j] * inv_T;
+      const float key = t + gumbel_noise(seed, (base | static_cast<uint32_t>(j)) + 1);
+      if (best < 0 || key > bk) { best = j; bk = key; }
+    }
+    return best;   // -1 only for a row of all -inf
+  };
+  for (int b = 0; b < batch; ++b) {
+    const int n = n_nodes[b];
+    if (n < 0 || n > B) return kBadTree;
+    const int32_t* par = parent + static_cast<size_t>(b) * B;
+    const int32_t* tk = token + static_cast<size_t>(b) * B;
+    for (int v = 0; v < n; ++v) {
+      if (par[v] < -1 || par[v] >= v) return kBadTree;
+      if (tk[v] < 0 || tk[v] >= vocab) return kBadToken;
+    }
+    const float* rows = target + static_cast<size_t>(b) * (B + 1) * vocab;
+    int32_t* at = acc_tokens + static_cast<size_t>(b) * n_depth;
+    int32_t* an = acc_nodes + static_cast<size_t>(b) * n_depth;
+    for (int i = 0; i < n_depth; ++i) { at[i] = -1; an[i] = -1; }
+    int cur = -1, r = 0, len = 0;
+    int a = draw(b, 0, rows);
+    while (true) {
+      int next = -1;
+      for (int c = 0; c < n; ++c)
+        if (par[c] == cur && tk[c] == a) { next = c; break; }
+      if (next < 0 || len >= n_depth) break;
+      at[len] = a;
+      an[len] = next;
+      ++len;
+      cur = next;
+      r = 1 + next;
+      a = draw(b, r, rows + static_cast<size_t>(r) * vocab);
+    }
+    acc_len[b] = len;
+    bonus[b] = a;
+  }
+  return 0;
+}
+
+// Test hooks for the pins: the log, the generator and the noise themselves.
+void orc_series_ln(const float* x, long n, float* out) {
+  for (long i = 0; i < n; ++i) out[i] = series_ln(x[i]);
+}
+void orc_splitmix64(uint64_t seed, const uint64_t* k, long n, uint64_t* out) {
+  for (long i = 0; i < n; ++i) out[i] = splitmix64_output(seed, k[i]);
+}
+void orc_gumbel(uint64_t seed, const uint64_t* k, long n, float* out) {
+  for (long i = 0; i < n; ++i) out[i] = gumbel_noise(seed, k[i]);
 }
 
 }  // extern "C"
