@@ -585,16 +585,24 @@ def main():
                                             entropy=ent[i % R], mode=jtree.JT_SCORE_HYBRID,
                                             alpha=0.5)
 
+    sampled_out = [{k: torch.empty_like(t) for k, t in bf.acc.items()} for bf in bufs]
+
+    def sampled_fn(i):
+        inp, bf = sets[i % R], bufs[i % R]
+        return lambda: jtree.jt_tree_accept(inp["target"], bf.tree["parent"], bf.tree["token"],
+                                            bf.tree["n_nodes"], w.N, out=sampled_out[i % R],
+                                            exec=ex, temperature=1.0, seed=1234 + i)
+
     next_ms = {}
     with torch.cuda.stream(stream):
         for i in range(R):
-            for fn in (commit_fn, entropy_fn, scored_fn):
+            for fn in (commit_fn, entropy_fn, scored_fn, sampled_fn):
                 fn(i)()
     stream.synchronize()
     if ex.read_error() != 0:
         raise RuntimeError("device error flag set by a next-row call")
     for name, fn in (("jt_tree_commit_kv", commit_fn), ("jt_topw_entropy", entropy_fn),
-                     ("jt_tree_expand_scored", scored_fn)):
+                     ("jt_tree_expand_scored", scored_fn), ("jt_tree_accept_sampled", sampled_fn)):
         g_c, ev_c = capture_fn(fn)
         torch.cuda.synchronize(dev)
         g_c.launch()
@@ -659,6 +667,10 @@ def main():
         "jt_tree_expand_scored": {
             "us": next_ms["jt_tree_expand_scored"] * 1e3,
             "note": "hybrid score (alpha 0.5) expansion; not in the step"},
+        "jt_tree_accept_sampled": {
+            "us": next_ms["jt_tree_accept_sampled"] * 1e3,
+            "note": ("temperature-1 acceptance (one Gumbel-max draw per visited node, "
+                     "counter-based noise for every logit it scans); not in the step")},
     }
 
     # ---- end to end through the public API with host buffers ---------------

@@ -269,6 +269,37 @@ JT_API jt_status jt_tree_accept(const float* target_logits, const int32_t* paren
                          int32_t* bonus, const jt_exec* exec);
 
 /* ------------------------------------------------------------------------
+ * jt_tree_accept_sampled — temperature-T (T > 0) acceptance.
+ * [PP] App. F.3 "Lossless verification": every committed token is the
+ * target's own draw at any temperature; a draft fixed before verification is
+ * checked with point-mass proposals, each draft token accepted with the
+ * target probability. [PP] App. F.1 gives the chain example: P(accept d1,
+ * reject d2, draw b) = p(d1) p(b | d1) = 0.24.
+ *
+ * Walk (this library's reading for trees; for a chain it is the rule above):
+ * at the current node draw y from softmax(target row / T); if a child has
+ * token y, accept it and continue from it; otherwise y is the bonus token.
+ * The draw is Gumbel-max, y = argmax_j (x_j * inv_T + G_j) (lowest j on
+ * ties) with inv_T = 1.0f / temperature in binary32 and counter-based noise:
+ *   k = ((b * (B+1) + r) << 32 | j) + 1   (r = 0: root row, 1+v: node v)
+ *   h = output k of SplitMix64 seeded with `seed`
+ *   U = ((h >> 41) + 0.5) * 2^-23,  G_j = -ln(-ln U)
+ * with ln evaluated by the atanh series in binary32 (so results are exactly
+ * reproducible from (seed, inputs)). The same seed on the same inputs gives
+ * the same walk; a caller draws a fresh seed per round.
+ * Arguments, outputs, limits, workspace (jt_tree_accept_workspace_bytes) and
+ * device checks as jt_tree_accept; temperature must be finite and > 0 (use
+ * jt_tree_accept for T = 0). A row whose logits are all -inf has no
+ * distribution and gives an unspecified token.
+ * ------------------------------------------------------------------------ */
+JT_API jt_status jt_tree_accept_sampled(const float* target_logits, const int32_t* parent,
+                                        const int32_t* token, const int32_t* n_nodes, int batch,
+                                        int B, int n_depth, int vocab, float temperature,
+                                        uint64_t seed, int32_t* acc_len, int32_t* acc_tokens,
+                                        int32_t* acc_nodes, int32_t* bonus,
+                                        const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
  * jt_tree_accept_noalloc — jt_tree_accept for callers that cannot allocate.
  * The paper has no counterpart: this is a library convenience.
  *

@@ -21,13 +21,15 @@
 //    per sequence walks, each step a warp-wide search for the matching child
 //    (__reduce_min_sync picks the lowest id).
 #include "jt_rowscan.cuh"
+#include "jt_sample.cuh"
 
 namespace jt {
 namespace {
 
+template <bool SAMPLED>
 __global__ void __launch_bounds__(kScanThreads)
 accept_argmax_kernel(const float* __restrict__ target, const int32_t* __restrict__ n_nodes,
-                     int B, int V, int S, int32_t* __restrict__ am) {
+                     int B, int V, int S, float inv_t, uint64_t seed, int32_t* __restrict__ am) {
   __shared__ ScanPartial<1> warp_parts[kScanWarps];
   __shared__ ScanPartial<1> part;
   const int row = blockIdx.x / S;
@@ -44,7 +46,11 @@ accept_argmax_kernel(const float* __restrict__ target, const int32_t* __restrict
   top.init();
   Lse lse;
   lse.init();
-  scan_segment<1, false>(target + (size_t)row * V, lo, hi, top, lse);
+  if (SAMPLED)
+    scan_segment<1, false, false, GumbelKeys>(target + (size_t)row * V, lo, hi, top, lse,
+                                              GumbelKeys{seed, (uint64_t)row << 32, inv_t});
+  else
+    scan_segment<1, false>(target + (size_t)row * V, lo, hi, top, lse);
   block_reduce<1, false>(top, lse, &part, warp_parts);
   if (cluster_reduce<1, false>(&part, S, top, lse)) am[row] = top.i[0];
 }
@@ -119,10 +125,12 @@ struct ArgPart {
   int i;
 };
 
+template <bool SAMPLED>
 __global__ void __launch_bounds__(kPathThreads)
 accept_path_kernel(const float* __restrict__ target, const int32_t* __restrict__ parent,
                    const int32_t* __restrict__ token, const int32_t* __restrict__ n_nodes, int B,
-                   int N, int V, int S, int prefetch, int32_t* __restrict__ acc_len,
+                   int N, int V, int S, int prefetch, float inv_t, uint64_t seed,
+                   int32_t* __restrict__ acc_len,
                    int32_t* __restrict__ acc_tokens, int32_t* __restrict__ acc_nodes,
                    int32_t* __restrict__ bonus, int32_t* d_err) {
   __shared__ int32_t par_s[kMaxB], tok_s[kMaxB];
@@ -170,6 +178,7 @@ accept_path_kernel(const float* __restrict__ target, const int32_t* __restrict__
       prefetch_l2_bulk(rows + (size_t)(1 + tid) * V + 4 * lo, (uint32_t)(hi - lo) * 16u);
     // Scan this CTA's segment of the current row: max, lowest index on ties.
     const float4* r4 = reinterpret_cast<const float4*>(rows + (size_t)row * V);
+    const GumbelKeys gk{seed, ((uint64_t)b * (B + 1) + row) << 32, inv_t};
     float bv = -INFINITY;
     int bi = INT_MAX;
     for (int j0 = lo + tid; j0 < hi; j0 += 4 * kPathThreads) {
@@ -178,6 +187,11 @@ accept_path_kernel(const float* __restrict__ target, const int32_t* __restrict__
       for (int u = 0; u < 4; ++u) {
         const int j = j0 + u * kPathThreads;
         x[u] = j < hi ? ld_stream(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      if (SAMPLED) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (j0 + u * kPathThreads < hi) x[u] = gk(x[u], j0 + u * kPathThreads);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -247,22 +261,25 @@ size_t accept_workspace_bytes(int batch, int B, int n_depth, int vocab) {
 cudaError_t launch_tree_accept(const Ctx& c, const float* target, const int32_t* parent,
                                const int32_t* token, const int32_t* n_nodes, int batch, int B,
                                int n_depth, int vocab, int32_t* acc_len, int32_t* acc_tokens,
-                               int32_t* acc_nodes, int32_t* bonus) {
+                               int32_t* acc_nodes, int32_t* bonus, bool sampled, float inv_t,
+                               uint64_t seed) {
   if (batch == 0) return cudaSuccess;
   if (use_path_walk(B, n_depth)) {
     // Cluster size: enough CTAs for ~4 per SM, at most 16 per sequence.
     int S = 1;
     while (S < 16 && (long)batch * S * 2 <= 4L * c.num_sms && (vocab / 4) / (2 * S) >= 1024) S *= 2;
     const int prefetch = (long)batch * B <= 64L * 64 ? 1 : 0;
-    return launch_kernel(accept_path_kernel, dim3(batch * S), dim3(kPathThreads), 0, c.stream, S,
-                         target, parent, token, n_nodes, B, n_depth, vocab, S, prefetch, acc_len,
+    auto kern = sampled ? accept_path_kernel<true> : accept_path_kernel<false>;
+    return launch_kernel(kern, dim3(batch * S), dim3(kPathThreads), 0, c.stream, S, target, parent,
+                         token, n_nodes, B, n_depth, vocab, S, prefetch, inv_t, seed, acc_len,
                          acc_tokens, acc_nodes, bonus, c.d_err);
   }
   int32_t* am = static_cast<int32_t*>(c.workspace);
   const long rows = (long)batch * (B + 1);
   const int S = pick_row_split(rows, vocab / 4, c.num_sms, 16);
-  cudaError_t e = launch_clustered(accept_argmax_kernel, (int)(rows * S), S, c.stream, target,
-                                   n_nodes, B, vocab, S, am);
+  auto kern = sampled ? accept_argmax_kernel<true> : accept_argmax_kernel<false>;
+  cudaError_t e = launch_clustered(kern, (int)(rows * S), S, c.stream, target, n_nodes, B, vocab,
+                                   S, inv_t, seed, am);
   if (e != cudaSuccess) return e;
   return launch_kernel(accept_walk_kernel, dim3((batch + kWalkWarps - 1) / kWalkWarps),
                        dim3(kWalkWarps * 32), 0, c.stream, 1, am, parent, token, n_nodes, batch, B,

@@ -231,10 +231,12 @@ size_t jt_tree_accept_workspace_bytes(int batch, int B, int n_depth, int vocab) 
   return accept_workspace_bytes(batch, B, n_depth, vocab);
 }
 
-jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, const int32_t* token,
-                         const int32_t* n_nodes, int batch, int B, int n_depth, int vocab,
-                         int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes,
-                         int32_t* bonus, const jt_exec* exec) {
+namespace {
+
+jt_status accept_impl(const float* target_logits, const int32_t* parent, const int32_t* token,
+                      const int32_t* n_nodes, int batch, int B, int n_depth, int vocab,
+                      int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus,
+                      bool sampled, float inv_t, uint64_t seed, const jt_exec* exec) {
   if (batch < 0 || B < 1 || B > kMaxB || n_depth < 1 || n_depth > kMaxDepth || vocab < 1)
     return JT_ERR_INVALID_ARG;
   if (vocab % 4 != 0) return JT_ERR_UNSUPPORTED;
@@ -251,7 +253,30 @@ jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, cons
   st = need_workspace(c, accept_workspace_bytes(batch, B, n_depth, vocab));
   if (st != JT_OK) return st;
   return from_cuda(launch_tree_accept(c, target_logits, parent, token, n_nodes, batch, B, n_depth,
-                                      vocab, acc_len, acc_tokens, acc_nodes, bonus));
+                                      vocab, acc_len, acc_tokens, acc_nodes, bonus, sampled,
+                                      inv_t, seed));
+}
+
+}  // namespace
+
+jt_status jt_tree_accept(const float* target_logits, const int32_t* parent, const int32_t* token,
+                         const int32_t* n_nodes, int batch, int B, int n_depth, int vocab,
+                         int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes,
+                         int32_t* bonus, const jt_exec* exec) {
+  return accept_impl(target_logits, parent, token, n_nodes, batch, B, n_depth, vocab, acc_len,
+                     acc_tokens, acc_nodes, bonus, false, 1.0f, 0, exec);
+}
+
+jt_status jt_tree_accept_sampled(const float* target_logits, const int32_t* parent,
+                                 const int32_t* token, const int32_t* n_nodes, int batch, int B,
+                                 int n_depth, int vocab, float temperature, uint64_t seed,
+                                 int32_t* acc_len, int32_t* acc_tokens, int32_t* acc_nodes,
+                                 int32_t* bonus, const jt_exec* exec) {
+  if (!(temperature > 0.0f) || !(temperature <= 3.0e38f)) return JT_ERR_INVALID_ARG;
+  const float inv_t = 1.0f / temperature;   // binary32 reciprocal, the multiplier of every key
+  if (!(inv_t <= 3.0e38f)) return JT_ERR_INVALID_ARG;
+  return accept_impl(target_logits, parent, token, n_nodes, batch, B, n_depth, vocab, acc_len,
+                     acc_tokens, acc_nodes, bonus, true, inv_t, seed, exec);
 }
 
 }  // extern "C"

@@ -87,7 +87,8 @@ size_t accept_workspace_bytes(int batch, int B, int n_depth, int vocab);
 cudaError_t launch_tree_accept(const Ctx&, const float* target, const int32_t* parent,
                                const int32_t* token, const int32_t* n_nodes, int batch, int B,
                                int n_depth, int vocab, int32_t* acc_len, int32_t* acc_tokens,
-                               int32_t* acc_nodes, int32_t* bonus);
+                               int32_t* acc_nodes, int32_t* bonus, bool sampled = false,
+                               float inv_t = 1.0f, uint64_t seed = 0);
 cudaError_t launch_tree_commit(const Ctx&, const jt_commit_args& a);
 size_t attn_workspace_bytes(const jt_attn_args& a, int num_sms);
 cudaError_t launch_tree_attn(const Ctx&, const jt_attn_args& a);

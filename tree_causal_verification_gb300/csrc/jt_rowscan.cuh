@@ -128,6 +128,12 @@ struct Lse {
   }
 };
 
+// Element transform applied to each float4 as it is loaded (float4 index j4):
+// the identity for plain scans.
+struct IdentityXf {
+  __device__ __forceinline__ float4 operator()(float4 x, int) const { return x; }
+};
+
 __device__ __forceinline__ float4 ld_stream(const float4* p) {
   float4 r;
   asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
@@ -232,9 +238,9 @@ __device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0
 // Streams float4s [lo4, hi4) of `row` into per-thread state: full batches
 // without bounds checks, ping-ponging two register buffers so that one batch
 // is in flight while the other is processed, then a checked tail.
-template <int K, bool LSE, bool ENT = false>
+template <int K, bool LSE, bool ENT = false, class Xf = IdentityXf>
 __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int lo4, int hi4,
-                                             TopK<K>& top, Lse& lse) {
+                                             TopK<K>& top, Lse& lse, const Xf& xf = Xf()) {
   const float4* r4 = reinterpret_cast<const float4*>(row);
   constexpr int STEP = kScanThreads * kScanBatch;
   const int tid = (int)threadIdx.x;
@@ -255,6 +261,8 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) b[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
     }
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) a[u] = xf(a[u], base + tid + u * kScanThreads);
     scan_batch<K, LSE, ENT>(a, base + tid, top, lse, refresh());
     base += STEP;
     if (!nb) break;
@@ -263,6 +271,8 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) a[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
     }
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) b[u] = xf(b[u], base + tid + u * kScanThreads);
     scan_batch<K, LSE, ENT>(b, base + tid, top, lse, refresh());
     base += STEP;
     if (!na) break;
@@ -274,7 +284,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u) {
       const int j = full_end + tid + u * kScanThreads;
-      a[u] = j < hi4 ? ld_stream(r4 + j) : ninf;
+      a[u] = j < hi4 ? xf(ld_stream(r4 + j), j) : ninf;
     }
     if (full_end + tid < hi4) {
       // Lanes whose whole batch is padding skip it (their padding would

@@ -34,7 +34,8 @@ STATUS_NAMES = {0: "JT_OK", 1: "JT_ERR_INVALID_ARG", 2: "JT_ERR_UNSUPPORTED", 3:
 EXPORTED = ["jt_status_str", "jt_read_device_error", "jt_topw_workspace_bytes", "jt_topw",
             "jt_tree_expand", "jt_tree_mask", "jt_tree_attn_workspace_bytes", "jt_tree_attn",
             "jt_tree_accept_workspace_bytes", "jt_tree_accept", "jt_tree_accept_noalloc",
-            "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored"]
+            "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored",
+            "jt_tree_accept_sampled"]
 JT_SCORE_LOGP, JT_SCORE_HYBRID, JT_SCORE_ENTROPY = 0, 1, 2
 
 
@@ -110,10 +111,14 @@ def load(path: str = LIB_PATH):
             lib.jt_tree_accept.argtypes = [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                            _vp, _vp, _vp, _vp, _pexec]
             lib.jt_tree_accept_noalloc.argtypes = lib.jt_tree_accept.argtypes
+            lib.jt_tree_accept_sampled.argtypes = [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                                   _c_int, ctypes.c_float, ctypes.c_uint64, _vp,
+                                                   _vp, _vp, _vp, _pexec]
             lib.jt_tree_commit_kv.argtypes = [ctypes.POINTER(jt_commit_args), _pexec]
             for name in ("jt_read_device_error", "jt_topw", "jt_tree_expand", "jt_tree_mask",
                          "jt_tree_attn", "jt_tree_accept", "jt_tree_accept_noalloc",
-                         "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored"):
+                         "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored",
+                         "jt_tree_accept_sampled"):
                 getattr(lib, name).restype = _c_int
             _lib = lib
     return _lib
@@ -314,8 +319,12 @@ def jt_tree_attn(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, mask,
     return out
 
 
-def jt_tree_accept(target, parent, token, n_nodes, n_depth, out=None, exec=None):
-    """Greedy acceptance; returns dict(acc_len, acc_tokens, acc_nodes, bonus)."""
+def jt_tree_accept(target, parent, token, n_nodes, n_depth, out=None, exec=None,
+                   temperature=0.0, seed=0):
+    """Acceptance; returns dict(acc_len, acc_tokens, acc_nodes, bonus).
+
+    temperature 0: greedy (jt_tree_accept); > 0: one target draw per visited
+    node from the counter-based stream `seed` (jt_tree_accept_sampled)."""
     batch, B = parent.shape
     V = target.shape[-1]
     dev = target.device
@@ -331,10 +340,16 @@ def jt_tree_accept(target, parent, token, n_nodes, n_depth, out=None, exec=None)
     lib = load()
     ex = _exec(exec).reserve(lib.jt_tree_accept_workspace_bytes(batch, B, n_depth, V))
     c = ex.c()
-    _check(lib.jt_tree_accept(_ptr(target), _ptr(parent), _ptr(token), _ptr(n_nodes), batch, B,
-                              n_depth, V, _ptr(out["acc_len"]), _ptr(out["acc_tokens"]),
-                              _ptr(out["acc_nodes"]), _ptr(out["bonus"]), ctypes.byref(c)),
-           "jt_tree_accept")
+    outs = (_ptr(out["acc_len"]), _ptr(out["acc_tokens"]), _ptr(out["acc_nodes"]),
+            _ptr(out["bonus"]))
+    if temperature == 0.0:
+        _check(lib.jt_tree_accept(_ptr(target), _ptr(parent), _ptr(token), _ptr(n_nodes), batch,
+                                  B, n_depth, V, *outs, ctypes.byref(c)), "jt_tree_accept")
+    else:
+        _check(lib.jt_tree_accept_sampled(_ptr(target), _ptr(parent), _ptr(token), _ptr(n_nodes),
+                                          batch, B, n_depth, V, ctypes.c_float(temperature),
+                                          ctypes.c_uint64(int(seed) & (2 ** 64 - 1)), *outs,
+                                          ctypes.byref(c)), "jt_tree_accept_sampled")
     return out
 
 
