@@ -212,11 +212,14 @@ JT_API jt_status jt_tree_mask(const int32_t* parent, const int32_t* n_nodes, int
  *   out          bf16 [batch][B][hq][D]
  *   scale        > 0; 0 means 1/sqrt(D)
  * Limits: D in {64, 128}; hq % hkv == 0; hq/hkv in {1, 2, 4, 8, 16}; 1 <= B <= 256;
- * page_size == 16 when paged. Workspace: jt_tree_attn_workspace_bytes. When
- * the (sequence, KV head, 256-row block) work units are too few to fill the
- * GPU, the key range of each unit is split over a cluster of up to 8 CTAs
- * whose fp32 partial outputs meet in this scratch: at most SM count x
- * (256 D + 1024) x 4 bytes; 0 when no split can apply.
+ * page_size == 16 when paged. Workspace: jt_tree_attn_workspace_bytes. Work
+ * is cut into (sequence, KV head, 256-row block) units. When two CTAs per unit
+ * fit on the SMs at once, each unit's key range is split over a cluster of up
+ * to 8 CTAs whose fp32 partial outputs meet in this scratch (at most SM count
+ * x (256 D + 1024) x 4 bytes; 0 when no split can apply). Otherwise the
+ * units run longest first (an order of 8 bytes per unit in the scratch), and
+ * while units are fewer than twice the SMs the long ones are cut into up to
+ * ceil(2 SMs / units) chunks with one (256 D + 512) x 4-byte partial each.
  * Device checks: prefix_len beyond max_prefix (or max_pages*page_size), a page
  * id outside [0, n_pages) and n_nodes outside [0, B] set flags; the affected
  * sequence's output is zero.

@@ -80,12 +80,17 @@ def _attn_args(batch, B, hq, hkv, D, max_prefix):
 def test_attn_workspace_query(lib):
     # Few work units (one sequence, 8 KV heads, one 256-row block each): the key
     # range is split over a cluster and the fp32 partials need scratch, bounded
-    # by one partial per SM. Many units (64 sequences x 4 KV heads x 1 block)
-    # fill the GPU without a split: no scratch.
+    # by one partial per SM. Many units (64 sequences x 4 KV heads x 4 blocks
+    # of 32 nodes x 8 heads) cover the SMs more than twice: no split, only the
+    # length order of the units (8 bytes per unit).
     small = lib.jt_tree_attn_workspace_bytes(ctypes.byref(_attn_args(1, 16, 32, 8, 128, 2048)))
     assert small > 0 and small % 256 == 0
     assert small <= 1024 * (256 * 128 + 1024) * 4
     assert lib.jt_tree_attn_workspace_bytes(
-        ctypes.byref(_attn_args(64, 128, 32, 4, 128, 16384))) == 0
+        ctypes.byref(_attn_args(64, 128, 32, 4, 128, 16384))) == 64 * 4 * 4 * 8
+    # In between (96 units), long units are cut into chunks: one partial per
+    # chunk slot on top of the order.
+    mid = lib.jt_tree_attn_workspace_bytes(ctypes.byref(_attn_args(24, 64, 16, 4, 128, 3000)))
+    assert mid >= 96 * 8 + 96 * 2 * (256 * 128 + 512) * 4
     # A single key tile cannot be split.
     assert lib.jt_tree_attn_workspace_bytes(ctypes.byref(_attn_args(1, 16, 32, 8, 128, 0))) == 0

@@ -210,3 +210,51 @@ def test_empty_batch_and_host_validation():
         jtree.jt_tree_expand(torch.zeros((1, 2, 2), dtype=torch.int32, device=DEV),
                              torch.zeros((1, 2, 2), dtype=torch.float32, device=DEV), 300)
     assert ex.read_error() == 0
+
+
+# Many units (sequence x KV head x 256-row block): the length-ordered schedule.
+# 96 units -> up to 4 chunks per unit merged by the last chunk to finish;
+# 320 units -> one CTA per unit, longest first. Ragged prefixes (0, 1, page
+# and tile edges, long), n_nodes 0 / 1 / B, paged and contiguous; all rows
+# of a few sequences plus a random sample of the rest are compared.
+@pytest.mark.parametrize("batch,hq,hkv,B,paged,Lmax", [(24, 16, 4, 64, True, 3000),
+                                                       (24, 16, 4, 64, False, 2100),
+                                                       (80, 8, 4, 16, True, 1500)])
+def test_attention_balanced_schedule(batch, hq, hkv, B, paged, Lmax):
+    rng = np.random.default_rng(batch + hq + B + paged)
+    g = torch.Generator().manual_seed(batch * 3 + B)
+    D = 128
+    n = rng.integers(0, B + 1, batch).astype(np.int32)
+    n[:3] = [B, 0, 1]
+    lens = rng.integers(0, Lmax + 1, batch).astype(np.int32)
+    lens[:6] = [Lmax, 0, 1, 127, 128, 129]
+    parent = np.stack([random_tree(rng, B, int(n[b])) for b in range(batch)])
+    mask = oracle.tree_mask(parent, n)
+    q = bf16((batch, B, hq, D), g)
+    kt, vt = bf16((batch, B, hkv, D), g), bf16((batch, B, hkv, D), g)
+    if paged:
+        max_pages = (Lmax + 15) // 16
+        n_pages = batch * max_pages + 3
+        bt = rng.permutation(n_pages)[: batch * max_pages].reshape(batch, max_pages).astype(np.int32)
+        kc, vc = bf16((n_pages, 16, hkv, D), g), bf16((n_pages, 16, hkv, D), g)
+    else:
+        bt = None
+        kc, vc = bf16((batch, Lmax, hkv, D), g), bf16((batch, Lmax, hkv, D), g)
+    d = lambda t: t.to(DEV)
+    ex = jtree.Exec(DEV)
+    out = jtree.jt_tree_attn(d(q), d(kt), d(vt), d(kc), d(vc), d(torch.from_numpy(lens)),
+                             d(torch.from_numpy(n)), d(torch.from_numpy(mask.view(np.int32))),
+                             block_table=None if bt is None else d(torch.from_numpy(bt)), exec=ex)
+    assert ex.read_error() == 0
+    rows = [(b, v, h) for b in (0, 1, 2) for v in range(B) for h in range(hq)]
+    rows += [(int(b), int(v), int(h)) for b, v, h in
+             zip(rng.integers(0, batch, 1500), rng.integers(0, B, 1500), rng.integers(0, hq, 1500))]
+    rows = np.array(rows, np.int32)
+    ref = oracle.tree_attn(q, kt, vt, kc, vc, lens, n, mask, hq=hq, hkv=hkv, block_table=bt,
+                           rows=rows)
+    got = out.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    check_attn(got, ref)
+    # Rows of unused budget slots are exactly zero.
+    o = out.float().cpu().numpy()
+    for b in range(batch):
+        assert not o[b, n[b]:].any()

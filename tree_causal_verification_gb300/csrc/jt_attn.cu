@@ -49,6 +49,7 @@
 #include <cooperative_groups.h>
 #include <cuda.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "jt_internal.cuh"
@@ -71,6 +72,15 @@ constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnParams {
   int batch, B, hq, hkv, g, npt, n_mpairs, S;
+  // Balanced schedule (kernel template flag BAL): block i runs work item
+  // perm[i] = unit * S + chunk (items sorted by length, longest first, -1
+  // past the last); a unit of t tiles is cut into min(S, ceil(t /
+  // chunk_tiles)) chunks whose partials the last chunk to finish merges
+  // (counters[unit] counts them). Otherwise unit = blockIdx / S and the S
+  // CTAs of a cluster split its key tiles.
+  int units, chunk_tiles;
+  int32_t* perm;
+  int32_t* counters;
   int paged, max_pages, n_pages, Lbound, words;
   const int32_t* block_table;
   const int32_t* prefix_len;
@@ -94,7 +104,15 @@ struct Bars {
   uint64_t s_full[2], p_full[2], pv_done[2], drain;
   uint32_t tmem_base;
   int abort;
+  int last;   // balanced schedule: this CTA finished its unit's last chunk
+  int unit, rank, split;   // this CTA's work, reloaded by the epilogue
 };
+
+// The epilogue reloads the CTA's coordinates from shared memory instead of
+// keeping them live in registers through the main loop.
+__device__ __forceinline__ int ld_shared_volatile(const int* p) {
+  return *reinterpret_cast<const volatile int*>(p);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 two = __floats2bfloat162_rn(lo, hi);
@@ -180,7 +198,126 @@ __device__ __forceinline__ void merge_split(const AttnParams& p, const float* pa
   }
 }
 
+// Balanced schedule: merge the k (<= 8) chunk partials of one unit, all of
+// its rows, in one CTA; same formula as merge_split. Partials are row-ordered
+// (slot = row), read past L1.
 template <int D>
+__device__ __forceinline__ void merge_chunks(const AttnParams& p, const float* part0, int k,
+                                             int n_live, int v0, int b, int kh, int tid,
+                                             float* fac /* [256][8] */) {
+  constexpr int PF = part_floats<D>();
+  const int g = p.g;
+  for (int r = tid; r < n_live; r += kThreads) {
+    float ms[8], ls[8];
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) {
+      ms[s2] = s2 < k ? __ldcg(part0 + (size_t)s2 * PF + 2 * kTile * D + r) : -INFINITY;
+      ls[s2] = s2 < k ? __ldcg(part0 + (size_t)s2 * PF + 2 * kTile * D + 2 * kTile + r) : 0.0f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) M = fmaxf(M, ms[s2]);
+    float lsum = 0.0f, f[8];
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) {
+      f[s2] = (ms[s2] == -INFINITY) ? 0.0f : ex2(ms[s2] - M);
+      lsum += f[s2] * ls[s2];
+    }
+    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) fac[r * 8 + s2] = f[s2] * inv;
+  }
+  __syncthreads();
+  // Item = (row r, float4 column c4), rows fastest: each load of a partial is
+  // one contiguous run per warp.
+  const float4* src0 = reinterpret_cast<const float4*>(part0);
+  for (int i = tid; i < n_live * (D / 4); i += kThreads) {
+    const int r = i % n_live, c4 = i / n_live;
+    float4 x[8];
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2)
+      if (s2 < k) x[s2] = __ldcg(src0 + (size_t)s2 * (PF / 4) + c4 * (2 * kTile) + r);
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) {
+      if (s2 < k) {
+        const float f = fac[r * 8 + s2];
+        acc.x += f * x[s2].x; acc.y += f * x[s2].y; acc.z += f * x[s2].z; acc.w += f * x[s2].w;
+      }
+    }
+    const int vv = v0 + r / g, jh = r % g;
+    reinterpret_cast<uint2*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[c4] =
+        make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  }
+  // Rows of unused budget slots (node < B): zeros.
+  for (int i = tid; i < (2 * kTile - n_live) * (D / 8); i += kThreads) {
+    const int r = n_live + i / (D / 8);
+    const int vv = v0 + r / g, jh = r % g;
+    if (vv < p.B)
+      reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[i % (D / 8)] =
+          make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Balanced schedule, before the attention grid: list the work items (unit,
+// chunk) of every unit, chunk count min(S, ceil(t / chunk_tiles)) for a unit
+// of t key tiles, sorted by chunk length, longest first (bitonic sort of
+// (length, item) keys in shared memory; unsorted beyond kPlanMaxSort slots),
+// into perm[0 .. units*S), -1 past the last item; and zero the chunk
+// counters. The counts only order the work: the attention kernel recomputes
+// and validates everything itself (it can only find fewer chunks, never
+// more, so every chunk it runs has an item).
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanMaxSort = 8192;
+
+__global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParams p) {
+  extern __shared__ unsigned long long keys[];
+  grid_dependency_sync();
+  const int units = p.units, S = p.S, slots = units * S, tid = threadIdx.x;
+  const bool sort = slots <= kPlanMaxSort;
+  int n2 = 1;
+  while (n2 < slots) n2 <<= 1;
+  if (sort) {
+    for (int i = tid; i < n2; i += kPlanThreads) {
+      unsigned long long key = ~0ull;
+      if (i < slots) {
+        const int u = i / S, c = i % S;
+        const int mp = u % p.n_mpairs, b = (u / p.n_mpairs) / p.hkv;
+        const int n = p.n_nodes[b], L = p.prefix_len[b];
+        int t = 0;
+        if (n >= 0 && n <= p.B && L >= 0 && L <= p.Lbound) {
+          const int v0 = mp * 2 * p.npt;
+          if (v0 < n) t = (L + kTile - 1) / kTile + (min(v0 + 2 * p.npt, n) - 1 + kTile) / kTile;
+        }
+        const int k = min(S, max(1, (t + p.chunk_tiles - 1) / p.chunk_tiles));
+        if (c < k) {
+          const int len = min((t + k - 1) / k, 0xFFFF);
+          key = ((unsigned long long)(0xFFFFu - (unsigned)len) << 32) | (unsigned)i;
+        }
+      }
+      keys[i] = key;
+    }
+    __syncthreads();
+    for (int k = 2; k <= n2; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < n2; i += kPlanThreads) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const unsigned long long a = keys[i], c = keys[ixj];
+            if ((a > c) == ((i & k) == 0)) { keys[i] = c; keys[ixj] = a; }
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+  for (int i = tid; i < slots; i += kPlanThreads)
+    p.perm[i] = !sort ? i : keys[i] == ~0ull ? -1 : (int)(keys[i] & 0xFFFFFFFFull);
+  if (p.counters)
+    for (int i = tid; i < units; i += kPlanThreads) p.counters[i] = 0;
+}
+
+template <int D, bool BAL>
 __global__ void __launch_bounds__(kThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mkc,
                     const __grid_constant__ CUtensorMap mvc, const __grid_constant__ CUtensorMap mkt,
@@ -201,13 +338,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.S;
-  const int rank = (int)(blockIdx.x % (unsigned)S);
-  const int unit = (int)(blockIdx.x / (unsigned)S);
-  const int mp = unit % p.n_mpairs;
-  const int bk = unit / p.n_mpairs;
-  const int kh = bk % p.hkv, b = bk / p.hkv;
   const int g = p.g, npt = p.npt;
-  const int v0 = mp * 2 * npt;
+  // Cluster schedule: unit and rank come from the block index (recomputed
+  // wherever needed); balanced schedule (BAL): from the plan, after the wait.
+  int rank = (int)(blockIdx.x % (unsigned)S);
+  int unit = (int)(blockIdx.x / (unsigned)S);
 
   // ---- set-up (independent of the sequence's data, so it overlaps the
   // drain of the previous grid and the latency of the loads below):
@@ -236,13 +371,29 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
 
   grid_dependency_sync();
 
+  bool no_item = false;   // balanced schedule: a grid slot past the last item
+  if (BAL) {
+    const int item = p.perm[blockIdx.x];
+    no_item = item < 0 || item >= p.units * S;
+    unit = no_item ? 0 : item / S;
+    rank = no_item ? 0 : item % S;
+    if (tid == 0) {
+      bars->unit = unit;
+      bars->rank = rank;
+    }
+  }
+  const int mp = unit % p.n_mpairs;
+  const int bk = unit / p.n_mpairs;
+  const int kh = bk % p.hkv, b = bk / p.hkv;
+  const int v0 = mp * 2 * npt;
+
   // ---- validate the sequence (same verdict in every CTA of the sequence) ----
   const int n_raw = p.n_nodes[b];
   const int L = p.prefix_len[b];
   int flag = 0;
   if (n_raw < 0 || n_raw > p.B) flag |= JT_DEVERR_NNODES;
   if (L < 0 || L > p.Lbound) flag |= JT_DEVERR_PREFIX;
-  if (p.paged && !(flag & JT_DEVERR_PREFIX)) {
+  if (p.paged && !no_item && !(flag & JT_DEVERR_PREFIX)) {
     const int np = (L + kPageSize - 1) / kPageSize;
     for (int i = tid; i < np; i += kThreads) {
       const int pg = p.block_table[(size_t)b * p.max_pages + i];
@@ -252,6 +403,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   tc_fence_before();
   const int bad = __syncthreads_or(flag);   // also publishes the barriers and the TMEM base
   tc_fence_after();
+  if (BAL && no_item) {
+    if (warp == kWarpMMA) tmem_dealloc(bars->tmem_base, kTmemCols);
+    return;
+  }
   if (flag && rank == 0) raise_flag(p.d_err, flag);
   const int n = bad ? 0 : n_raw;
 
@@ -261,15 +416,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int v_last = min(v0 + 2 * npt, n) - 1;
   const int t_tree = has_rows ? (v_last + kTile) / kTile : 0;
   const int t_tot = p_tiles + t_tree;
-  const int t_begin = (int)((long)rank * t_tot / S);
-  const int t_end = (int)((long)(rank + 1) * t_tot / S);
+  // CTAs sharing this unit's key tiles: the cluster, or this unit's chunks.
+  const int split = BAL ? min(S, max(1, (t_tot + p.chunk_tiles - 1) / p.chunk_tiles)) : S;
+  if (BAL && tid == 0) bars->split = split;
+  if (BAL && rank >= split) {   // a chunk slot this unit does not need
+    if (warp == kWarpMMA) tmem_dealloc(bars->tmem_base, kTmemCols);
+    return;
+  }
+  const int t_begin = (int)((long)rank * t_tot / split);
+  const int t_end = (int)((long)(rank + 1) * t_tot / split);
   const int T = t_end - t_begin;
 
   if (!has_rows) {
     // Every row of this unit is an unused budget slot: zeros. The unit's
-    // CTAs split the rows; with a split they still join the cluster barrier.
+    // CTAs split the rows; in a cluster they still join its barrier.
     if (warp == kWarpMMA) tmem_dealloc(bars->tmem_base, kTmemCols);
-    const int R = 2 * kTile / S;
+    const int R = 2 * kTile / split;
     for (int i = tid; i < R * (D / 8); i += kThreads) {
       const int r = rank * R + i / (D / 8), u = i % (D / 8);
       const int v = v0 + r / g, j = r % g;
@@ -277,7 +439,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * g + j) * D)[u] =
             make_uint4(0, 0, 0, 0);
     }
-    if (S > 1) cg::this_cluster().sync();
+    if (!BAL && S > 1) cg::this_cluster().sync();
     return;
   }
 
@@ -582,20 +744,29 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   __syncthreads();
 
   // ---- output (S == 1) or publish partials (S > 1); both read O from TMEM ----
-  const int n_live = min(2 * kTile, (n - v0) * g);   // rows of live nodes come first
+  const int unit_e = BAL ? ld_shared_volatile(&bars->unit) : unit;
+  const int rank_e = BAL ? ld_shared_volatile(&bars->rank) : rank;
+  const int split_e = BAL ? ld_shared_volatile(&bars->split) : split;
+  const int bk_e = unit_e / p.n_mpairs;
+  const int kh_e = bk_e % p.hkv, b_e = bk_e / p.hkv;
+  const int v0_e = (unit_e % p.n_mpairs) * 2 * npt;
+  const int n_live = min(2 * kTile, (n - v0_e) * g);   // rows of live nodes come first
   if (warp < 8) {
     const int j = R % g;
     const bool write_row = v < p.B;
     const float inv = (v < n && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-    if (S > 1) {
+    if (split_e > 1) {
       // Only rows that some rank will merge are written; coalesced per column
       // (a warp's 32 rows land in 32 / S runs of whole 32-byte sectors). The
       // TMEM load is warp-collective, so the whole warp takes it whenever any
-      // of its rows is live, and only the stores are per row.
+      // of its rows is live, and only the stores are per row. The balanced
+      // schedule's single merging CTA reads rows in order (slot = R).
       if ((R & ~31) < n_live) {
         const bool live = R < n_live;
-        float* part = p.part + (size_t)blockIdx.x * part_floats<D>();
-        const int slot = (R % S) * (2 * kTile / S) + R / S;
+        const size_t pidx = BAL ? (size_t)unit_e * S + rank_e : (size_t)blockIdx.x;
+        float* part = p.part + pidx * part_floats<D>();
+        const int sig = BAL ? 1 : S;
+        const int slot = (R % sig) * (2 * kTile / sig) + R / sig;
         float4* po = reinterpret_cast<float4*>(part);
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -620,7 +791,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         }
       }
     } else {
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + v) * p.hq + kh * g + j) * D);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b_e * p.B + v) * p.hq + kh_e * g + j) * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
@@ -657,17 +828,30 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (S == 1) return;
+  if (split_e == 1) return;
+
+  if (BAL) {
+    // ---- the last chunk of the unit to finish merges all of them ----
+    __threadfence();   // this CTA's partial is visible device-wide ...
+    __syncthreads();   // ... before the count says so
+    if (tid == 0) bars->last = atomicAdd(&p.counters[unit_e], 1) == split_e - 1;
+    __syncthreads();
+    if (!bars->last) return;
+    __threadfence();
+    merge_chunks<D>(p, p.part + (size_t)unit_e * S * part_floats<D>(), split_e, n_live, v0_e,
+                    b_e, kh_e, tid, reinterpret_cast<float*>(sm));
+    return;
+  }
 
   // ---- split-KV merge through L2 (the cluster barrier, reached by every CTA
   // of the split, orders the partial writes above before the reads) ----
   cg::this_cluster().sync();
   float* fac = reinterpret_cast<float*>(sm);   // over the dead Q tile
-  const float* part0 = p.part + (size_t)(blockIdx.x - rank) * part_floats<D>();
+  const float* part0 = p.part + (size_t)(blockIdx.x - rank_e) * part_floats<D>();
   switch (S) {
-    case 2: merge_split<D, 2, 4>(p, part0, fac, rank, n_live, v0, b, kh, tid); break;
-    case 4: merge_split<D, 4, 2>(p, part0, fac, rank, n_live, v0, b, kh, tid); break;
-    default: merge_split<D, 8, 1>(p, part0, fac, rank, n_live, v0, b, kh, tid); break;
+    case 2: merge_split<D, 2, 4>(p, part0, fac, rank_e, n_live, v0_e, b_e, kh_e, tid); break;
+    case 4: merge_split<D, 4, 2>(p, part0, fac, rank_e, n_live, v0_e, b_e, kh_e, tid); break;
+    default: merge_split<D, 8, 1>(p, part0, fac, rank_e, n_live, v0_e, b_e, kh_e, tid); break;
   }
 }
 
@@ -744,23 +928,70 @@ int split_limit(const jt_attn_args& a, const AttnParams& p, int num_sms) {
   return s;
 }
 
+// Schedule choice, a function of the shapes only (so that the workspace
+// query and the launch agree). Few units (two or more CTAs per unit fit in
+// one wave): cluster split. Otherwise the balanced schedule, with up to
+// ceil(2 SMs / units) chunks per unit (1 when the units alone cover the SMs
+// twice) and chunks of ceil(tiles_max / S) tiles.
+struct Schedule {
+  int balanced, S, chunk_tiles, units;
+};
+
+Schedule pick_schedule(const jt_attn_args& a, const AttnParams& p, int num_sms) {
+  Schedule sc{0, 1, 0, a.batch * a.hkv * p.n_mpairs};
+  if ((long)sc.units * 2 <= num_sms) return sc;   // cluster split (S chosen at launch)
+  const int tiles_max = (p.Lbound + kTile - 1) / kTile + (a.B + kTile - 1) / kTile;
+  sc.balanced = 1;
+  sc.S = (int)std::min<long>(8, std::max<long>(1, (2L * num_sms + sc.units - 1) / sc.units));
+  sc.S = std::min(sc.S, std::max(1, tiles_max));
+  sc.chunk_tiles = std::max(1, (tiles_max + sc.S - 1) / sc.S);
+  return sc;
+}
+
+size_t balanced_meta_bytes(int units, int S) {
+  return align_up((size_t)units * (S + 1) * sizeof(int32_t), 256);   // items, then counters
+}
+
 template <int D>
 size_t smem_bytes() { return (2 + 2 * kStages) * (size_t)kTile * D * 2 + 256 + 1024; }
 
 template <int D>
 cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   const size_t smem = smem_bytes<D>();
-  auto kern = tree_attn_tc_kernel<D>;
+  const int units = a.batch * a.hkv * p.n_mpairs;
+  const Schedule sc = pick_schedule(a, p, c.num_sms);
+  auto kern = sc.balanced ? tree_attn_tc_kernel<D, true> : tree_attn_tc_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
 
-  const int units = a.batch * a.hkv * p.n_mpairs;
-  // Split the key tiles over S CTAs only when the workspace holds the partials.
-  const bool have_part = p.part != nullptr &&
+  if (sc.balanced) {
+    const size_t meta = balanced_meta_bytes(units, sc.S);
+    const size_t need = meta + (sc.S > 1 ? align_up((size_t)units * sc.S * part_floats<D>() *
+                                                        sizeof(float), 256) : 0);
+    if (!c.workspace || c.workspace_bytes < need) return cudaErrorInvalidValue;
+    p.units = units;
+    p.S = sc.S;
+    p.chunk_tiles = sc.chunk_tiles;
+    p.perm = static_cast<int32_t*>(c.workspace);
+    p.counters = sc.S > 1 ? p.perm + (size_t)units * sc.S : nullptr;
+    p.part = sc.S > 1 ? reinterpret_cast<float*>(static_cast<char*>(c.workspace) + meta) : nullptr;
+    int n2 = 1;
+    while (n2 < units * sc.S) n2 <<= 1;
+    const size_t plan_smem = units * sc.S <= kPlanMaxSort ? (size_t)n2 * 8 : 0;
+    if (plan_smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(attn_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)plan_smem);
+      if (e != cudaSuccess) return e;
+    }
+    e = launch_kernel(attn_plan_kernel, dim3(1), dim3(kPlanThreads), plan_smem, c.stream, 1, p);
+    if (e != cudaSuccess) return e;
+  }
+  // Cluster split: only when the workspace holds the partials.
+  const bool have_part = !sc.balanced && p.part != nullptr &&
                          c.workspace_bytes >= (size_t)c.num_sms * part_floats<D>() * sizeof(float);
   const int limit = have_part ? split_limit(a, p, c.num_sms) : 1;
   // Largest split whose clusters are all resident at once (one wave).
-  int S = 1;
+  int S = sc.balanced ? sc.S : 1;
   cudaLaunchConfig_t occ = {};
   cudaLaunchAttribute occ_attr[1];
   occ.blockDim = dim3(kThreads);
@@ -771,7 +1002,7 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   occ_attr[0].val.clusterDim.z = 1;
   occ.attrs = occ_attr;
   occ.numAttrs = 1;
-  for (int cand = 2; cand <= limit; cand *= 2) {
+  for (int cand = 2; !sc.balanced && cand <= limit; cand *= 2) {
     occ_attr[0].val.clusterDim.x = cand;
     occ.gridDim = dim3(units * cand);
     int nclusters = 0;
@@ -807,8 +1038,8 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
       !make_map(&mvt, a.v_tree, {D64, (uint64_t)a.hkv, (uint64_t)a.B, (uint64_t)a.batch},
                 {64, 1, (uint32_t)kTile, 1}))
     return cudaErrorInvalidValue;
-  return launch_kernel(kern, dim3(units * S), dim3(kThreads), smem, c.stream, S, mq, mkc, mvc, mkt,
-                       mvt, p);
+  return launch_kernel(kern, dim3(units * S), dim3(kThreads), smem, c.stream,
+                       sc.balanced ? 1 : S, mq, mkc, mvc, mkt, mvt, p);
 }
 
 }  // namespace
@@ -816,10 +1047,16 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
 size_t attn_workspace_bytes(const jt_attn_args& a, int num_sms) {
   if (a.batch == 0) return 0;
   AttnParams p = make_params(a);
-  // A split grid never exceeds the SMs (one CTA per SM, one wave), so
+  const size_t per = (a.head_dim == 64 ? part_floats<64>() : part_floats<128>()) * sizeof(float);
+  const Schedule sc = pick_schedule(a, p, num_sms);
+  if (sc.balanced) {
+    // unit order and chunk counters, then one partial per chunk slot
+    return balanced_meta_bytes(sc.units, sc.S) +
+           (sc.S > 1 ? align_up((size_t)sc.units * sc.S * per, 256) : 0);
+  }
+  // A cluster split never exceeds the SMs (one CTA per SM, one wave), so
   // num_sms partials always suffice; none are needed when no split fits.
   if (split_limit(a, p, num_sms) < 2) return 0;
-  const size_t per = (a.head_dim == 64 ? part_floats<64>() : part_floats<128>()) * sizeof(float);
   return align_up((size_t)num_sms * per, 256);
 }
 
