@@ -75,12 +75,12 @@ struct AttnParams {
   // Balanced schedule (kernel template flag BAL): block i runs work item
   // perm[i] = unit * S + chunk (items sorted by length, longest first, -1
   // past the last); a unit of t tiles is cut into min(S, ceil(t /
-  // chunk_tiles)) chunks whose partials the last chunk to finish merges
-  // (counters[unit] counts them). Otherwise unit = blockIdx / S and the S
-  // CTAs of a cluster split its key tiles.
+  // chunk_tiles)) chunks (nparts[unit], written by its chunk 0) whose
+  // partials attn_merge_kernel combines after the grid. Otherwise unit =
+  // blockIdx / S and the S CTAs of a cluster split its key tiles.
   int units, chunk_tiles;
   int32_t* perm;
-  int32_t* counters;
+  int32_t* nparts;
   int paged, max_pages, n_pages, Lbound, words;
   const int32_t* block_table;
   const int32_t* prefix_len;
@@ -104,7 +104,6 @@ struct Bars {
   uint64_t s_full[2], p_full[2], pv_done[2], drain;
   uint32_t tmem_base;
   int abort;
-  int last;   // balanced schedule: this CTA finished its unit's last chunk
   int unit, rank, split;   // this CTA's work, reloaded by the epilogue
 };
 
@@ -198,16 +197,73 @@ __device__ __forceinline__ void merge_split(const AttnParams& p, const float* pa
   }
 }
 
-// Balanced schedule: merge the k (<= 8) chunk partials of one unit, all of
-// its rows, in one CTA; same formula as merge_split. Partials are row-ordered
-// (slot = row), read past L1.
+// Balanced schedule, after the attention grid: combine the k = nparts[unit]
+// (<= 8) chunk partials of every split unit with the same formula as
+// merge_split; kMergeSlices CTAs per unit, each a slice of its 256 rows, so
+// the merges of all units run side by side across the SMs. Partials are
+// row-ordered (slot = row) and read past L1; every thread keeps UN items x
+// KMAX loads in flight. Units with k < 2 wrote their output directly.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeSlices = 4;
+constexpr int kMergeRows = 2 * kTile / kMergeSlices;
+
+template <int D, int UN, int KMAX>
+__device__ __forceinline__ void merge_rows(const AttnParams& p, const float* part0, int k,
+                                           int r0, int r1, int v0, int b, int kh,
+                                           const float* fac) {
+  constexpr int PF4 = part_floats<D>() / 4;
+  const int g = p.g, rows = r1 - r0, items = rows * (D / 4);
+  const float4* src0 = reinterpret_cast<const float4*>(part0);
+  for (int i0 = threadIdx.x; i0 < items; i0 += UN * kMergeThreads) {
+    float4 x[UN][KMAX];
+#pragma unroll
+    for (int u = 0; u < UN; ++u) {
+      const int i = i0 + u * kMergeThreads;
+      if (i < items) {
+        const int r = r0 + i % rows, c4 = i / rows;
+#pragma unroll
+        for (int s2 = 0; s2 < KMAX; ++s2)
+          if (s2 < k) x[u][s2] = __ldcg(src0 + (size_t)s2 * PF4 + c4 * (2 * kTile) + r);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UN; ++u) {
+      const int i = i0 + u * kMergeThreads;
+      if (i < items) {
+        const int r = r0 + i % rows, c4 = i / rows;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int s2 = 0; s2 < KMAX; ++s2) {
+          if (s2 < k) {
+            const float f = fac[(r - r0) * 8 + s2];
+            acc.x += f * x[u][s2].x; acc.y += f * x[u][s2].y;
+            acc.z += f * x[u][s2].z; acc.w += f * x[u][s2].w;
+          }
+        }
+        const int vv = v0 + r / g, jh = r % g;
+        reinterpret_cast<uint2*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[c4] =
+            make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+      }
+    }
+  }
+}
+
 template <int D>
-__device__ __forceinline__ void merge_chunks(const AttnParams& p, const float* part0, int k,
-                                             int n_live, int v0, int b, int kh, int tid,
-                                             float* fac /* [256][8] */) {
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p) {
+  __shared__ float fac[kMergeRows * 8];
   constexpr int PF = part_floats<D>();
-  const int g = p.g;
-  for (int r = tid; r < n_live; r += kThreads) {
+  grid_dependency_sync();
+  const int unit = blockIdx.x / kMergeSlices, slice = blockIdx.x % kMergeSlices;
+  const int k = p.nparts[unit];
+  if (k < 2) return;   // no partials: the unit's output is already written
+  const int mp = unit % p.n_mpairs, bk = unit / p.n_mpairs;
+  const int kh = bk % p.hkv, b = bk / p.hkv;
+  const int g = p.g, v0 = mp * 2 * p.npt;
+  const int n = p.n_nodes[b];   // valid: a unit with partials passed the checks
+  const int n_live = min(2 * kTile, (n - v0) * g);
+  const int r0 = slice * kMergeRows, r1 = min(n_live, r0 + kMergeRows);
+  const float* part0 = p.part + (size_t)unit * p.S * PF;
+  for (int r = r0 + threadIdx.x; r < r1; r += kMergeThreads) {
     float ms[8], ls[8];
 #pragma unroll
     for (int s2 = 0; s2 < 8; ++s2) {
@@ -225,33 +281,18 @@ __device__ __forceinline__ void merge_chunks(const AttnParams& p, const float* p
     }
     const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
 #pragma unroll
-    for (int s2 = 0; s2 < 8; ++s2) fac[r * 8 + s2] = f[s2] * inv;
+    for (int s2 = 0; s2 < 8; ++s2) fac[(r - r0) * 8 + s2] = f[s2] * inv;
   }
   __syncthreads();
-  // Item = (row r, float4 column c4), rows fastest: each load of a partial is
-  // one contiguous run per warp.
-  const float4* src0 = reinterpret_cast<const float4*>(part0);
-  for (int i = tid; i < n_live * (D / 4); i += kThreads) {
-    const int r = i % n_live, c4 = i / n_live;
-    float4 x[8];
-#pragma unroll
-    for (int s2 = 0; s2 < 8; ++s2)
-      if (s2 < k) x[s2] = __ldcg(src0 + (size_t)s2 * (PF / 4) + c4 * (2 * kTile) + r);
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-    for (int s2 = 0; s2 < 8; ++s2) {
-      if (s2 < k) {
-        const float f = fac[r * 8 + s2];
-        acc.x += f * x[s2].x; acc.y += f * x[s2].y; acc.z += f * x[s2].z; acc.w += f * x[s2].w;
-      }
-    }
-    const int vv = v0 + r / g, jh = r % g;
-    reinterpret_cast<uint2*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[c4] =
-        make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  if (r1 > r0) {
+    if (k <= 2) merge_rows<D, 4, 2>(p, part0, k, r0, r1, v0, b, kh, fac);
+    else if (k <= 4) merge_rows<D, 2, 4>(p, part0, k, r0, r1, v0, b, kh, fac);
+    else merge_rows<D, 1, 8>(p, part0, k, r0, r1, v0, b, kh, fac);
   }
-  // Rows of unused budget slots (node < B): zeros.
-  for (int i = tid; i < (2 * kTile - n_live) * (D / 8); i += kThreads) {
-    const int r = n_live + i / (D / 8);
+  // This slice's rows of unused budget slots (node < B): zeros.
+  const int z0 = max(r0, n_live), z1 = r0 + kMergeRows;
+  for (int i = threadIdx.x; i < max(0, z1 - z0) * (D / 8); i += kMergeThreads) {
+    const int r = z0 + i / (D / 8);
     const int vv = v0 + r / g, jh = r % g;
     if (vv < p.B)
       reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[i % (D / 8)] =
@@ -263,8 +304,9 @@ __device__ __forceinline__ void merge_chunks(const AttnParams& p, const float* p
 // chunk) of every unit, chunk count min(S, ceil(t / chunk_tiles)) for a unit
 // of t key tiles, sorted by chunk length, longest first (bitonic sort of
 // (length, item) keys in shared memory; unsorted beyond kPlanMaxSort slots),
-// into perm[0 .. units*S), -1 past the last item; and zero the chunk
-// counters. The counts only order the work: the attention kernel recomputes
+// into perm[0 .. units*S), -1 past the last item; and zero the per-unit
+// partial counts (a unit whose chunk 0 never runs is then left alone by the
+// merge). The counts only order the work: the attention kernel recomputes
 // and validates everything itself (it can only find fewer chunks, never
 // more, so every chunk it runs has an item).
 constexpr int kPlanThreads = 1024;
@@ -313,8 +355,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
   }
   for (int i = tid; i < slots; i += kPlanThreads)
     p.perm[i] = !sort ? i : keys[i] == ~0ull ? -1 : (int)(keys[i] & 0xFFFFFFFFull);
-  if (p.counters)
-    for (int i = tid; i < units; i += kPlanThreads) p.counters[i] = 0;
+  if (p.nparts)
+    for (int i = tid; i < units; i += kPlanThreads) p.nparts[i] = 0;
 }
 
 template <int D, bool BAL>
@@ -418,7 +460,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int t_tot = p_tiles + t_tree;
   // CTAs sharing this unit's key tiles: the cluster, or this unit's chunks.
   const int split = BAL ? min(S, max(1, (t_tot + p.chunk_tiles - 1) / p.chunk_tiles)) : S;
-  if (BAL && tid == 0) bars->split = split;
+  if (BAL && tid == 0) {
+    bars->split = split;
+    if (rank == 0 && p.nparts) p.nparts[unit] = split;   // read by attn_merge_kernel
+  }
   if (BAL && rank >= split) {   // a chunk slot this unit does not need
     if (warp == kWarpMMA) tmem_dealloc(bars->tmem_base, kTmemCols);
     return;
@@ -830,18 +875,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   }
   if (split_e == 1) return;
 
-  if (BAL) {
-    // ---- the last chunk of the unit to finish merges all of them ----
-    __threadfence();   // this CTA's partial is visible device-wide ...
-    __syncthreads();   // ... before the count says so
-    if (tid == 0) bars->last = atomicAdd(&p.counters[unit_e], 1) == split_e - 1;
-    __syncthreads();
-    if (!bars->last) return;
-    __threadfence();
-    merge_chunks<D>(p, p.part + (size_t)unit_e * S * part_floats<D>(), split_e, n_live, v0_e,
-                    b_e, kh_e, tid, reinterpret_cast<float*>(sm));
-    return;
-  }
+  if (BAL) return;   // attn_merge_kernel combines the chunks after the grid
 
   // ---- split-KV merge through L2 (the cluster barrier, reached by every CTA
   // of the split, orders the partial writes above before the reads) ----
@@ -949,7 +983,7 @@ Schedule pick_schedule(const jt_attn_args& a, const AttnParams& p, int num_sms) 
 }
 
 size_t balanced_meta_bytes(int units, int S) {
-  return align_up((size_t)units * (S + 1) * sizeof(int32_t), 256);   // items, then counters
+  return align_up((size_t)units * (S + 1) * sizeof(int32_t), 256);   // items, then part counts
 }
 
 template <int D>
@@ -973,7 +1007,7 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
     p.S = sc.S;
     p.chunk_tiles = sc.chunk_tiles;
     p.perm = static_cast<int32_t*>(c.workspace);
-    p.counters = sc.S > 1 ? p.perm + (size_t)units * sc.S : nullptr;
+    p.nparts = sc.S > 1 ? p.perm + (size_t)units * sc.S : nullptr;
     p.part = sc.S > 1 ? reinterpret_cast<float*>(static_cast<char*>(c.workspace) + meta) : nullptr;
     int n2 = 1;
     while (n2 < units * sc.S) n2 <<= 1;
@@ -1038,8 +1072,11 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
       !make_map(&mvt, a.v_tree, {D64, (uint64_t)a.hkv, (uint64_t)a.B, (uint64_t)a.batch},
                 {64, 1, (uint32_t)kTile, 1}))
     return cudaErrorInvalidValue;
-  return launch_kernel(kern, dim3(units * S), dim3(kThreads), smem, c.stream,
-                       sc.balanced ? 1 : S, mq, mkc, mvc, mkt, mvt, p);
+  e = launch_kernel(kern, dim3(units * S), dim3(kThreads), smem, c.stream,
+                    sc.balanced ? 1 : S, mq, mkc, mvc, mkt, mvt, p);
+  if (e != cudaSuccess || !sc.balanced || sc.S < 2) return e;
+  return launch_kernel(attn_merge_kernel<D>, dim3(units * kMergeSlices), dim3(kMergeThreads), 0,
+                       c.stream, 1, p);
 }
 
 }  // namespace
@@ -1050,7 +1087,7 @@ size_t attn_workspace_bytes(const jt_attn_args& a, int num_sms) {
   const size_t per = (a.head_dim == 64 ? part_floats<64>() : part_floats<128>()) * sizeof(float);
   const Schedule sc = pick_schedule(a, p, num_sms);
   if (sc.balanced) {
-    // unit order and chunk counters, then one partial per chunk slot
+    // item order and per-unit part counts, then one partial per chunk slot
     return balanced_meta_bytes(sc.units, sc.S) +
            (sc.S > 1 ? align_up((size_t)sc.units * sc.S * per, 256) : 0);
   }
