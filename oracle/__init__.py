@@ -304,3 +304,26 @@ def tree_commit_kv(k_tree, v_tree, k_cache, v_cache, prefix_len, acc_len, acc_no
     if check:
         _check(rc, "orc_tree_commit_kv")
     return k_out, v_out, new_len, rc
+
+
+def lmhead_logits(hidden, w_lm):
+    """Draft logits through the LM head: hidden bf16 [rows][d] times w_lm bf16
+    [vocab][d] transposed, every product and sum in float64 from the exactly
+    widened bf16 values (a library matmul is the step), returned in float64."""
+    h = _widen_bf16(hidden)
+    w = _widen_bf16(w_lm)
+    return h @ w.T
+
+
+def lmhead_topw(hidden, w_lm, W):
+    """Top-W tokens and log-probs of softmax(hidden @ w_lm^T) per row, with the
+    logits rounded once to binary32 before the top-W step (orc_topw).
+    Returns (tok [rows][W], logp [rows][W], logits float64 [rows][vocab])."""
+    logits = lmhead_logits(hidden, w_lm)
+    tok, logp = topw(logits.astype(np.float32)[None], W)
+    return tok[0], logp[0], logits
+
+
+def _widen_bf16(a):
+    bits = _bf16_bits(a)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
