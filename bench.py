@@ -593,16 +593,33 @@ def main():
                                             bf.tree["n_nodes"], w.N, out=sampled_out[i % R],
                                             exec=ex, temperature=1.0, seed=1234 + i)
 
+    # Draft LM head fused with top-W: the draft's hidden states for this
+    # step's rows through a synthetic LM-head matrix of the target's shape
+    # (d 4096, the workload's vocabulary; random weights: timing only).
+    d_model = 4096
+    gl = torch.Generator(device=dev).manual_seed(4242)
+    w_lm = (torch.randn((w.V, d_model), generator=gl, device=dev) * 0.02).to(torch.bfloat16)
+    hid = [(torch.randn((w.batch * w.N, d_model), generator=gl, device=dev)).to(torch.bfloat16)
+           for _ in range(R)]
+    lm_tok = [torch.empty((w.batch * w.N, w.W), dtype=torch.int32, device=dev) for _ in range(R)]
+    lm_logp = [torch.empty((w.batch * w.N, w.W), dtype=torch.float32, device=dev)
+               for _ in range(R)]
+
+    def lmhead_fn(i):
+        return lambda: jtree.jt_lmhead_topw(hid[i % R], w_lm, w.W, tok=lm_tok[i % R],
+                                            logp=lm_logp[i % R], exec=ex)
+
     next_ms = {}
     with torch.cuda.stream(stream):
         for i in range(R):
-            for fn in (commit_fn, entropy_fn, scored_fn, sampled_fn):
+            for fn in (commit_fn, entropy_fn, scored_fn, sampled_fn, lmhead_fn):
                 fn(i)()
     stream.synchronize()
     if ex.read_error() != 0:
         raise RuntimeError("device error flag set by a next-row call")
     for name, fn in (("jt_tree_commit_kv", commit_fn), ("jt_topw_entropy", entropy_fn),
-                     ("jt_tree_expand_scored", scored_fn), ("jt_tree_accept_sampled", sampled_fn)):
+                     ("jt_tree_expand_scored", scored_fn), ("jt_tree_accept_sampled", sampled_fn),
+                     ("jt_lmhead_topw", lmhead_fn)):
         g_c, ev_c = capture_fn(fn)
         torch.cuda.synchronize(dev)
         g_c.launch()
@@ -655,6 +672,15 @@ def main():
         calls_out[c] = d
 
     topw_b = avg_work["jt_topw"]["bytes"] + w.batch * w.N * 4
+    lm_rows = w.batch * w.N
+    lm_bytes = w.V * d_model * 2 + lm_rows * d_model * 2 + lm_rows * w.W * 8
+    lm_flops = 2.0 * lm_rows * d_model * w.V
+    lm_s = next_ms["jt_lmhead_topw"] / 1e3
+    lm_row = {"us": lm_s * 1e6, "alg_bytes": lm_bytes, "alg_flops": lm_flops,
+              "hbm_frac": lm_bytes / lm_s / 1e9 / peaks["hbm_gbs"],
+              "tensor_frac": lm_flops / lm_s / (peaks["bf16_tflops"] * 1e12),
+              "note": ("draft hidden [batch*N][4096] x synthetic LM head [vocab][4096] bf16, "
+                       "top-W per row without writing logits; not in the step")}
     next_rows = {
         "jt_tree_commit_kv": {
             "us": commit_ms * 1e3, "alg_bytes": commit_bytes,
@@ -667,6 +693,7 @@ def main():
         "jt_tree_expand_scored": {
             "us": next_ms["jt_tree_expand_scored"] * 1e3,
             "note": "hybrid score (alpha 0.5) expansion; not in the step"},
+        "jt_lmhead_topw": lm_row,
         "jt_tree_accept_sampled": {
             "us": next_ms["jt_tree_accept_sampled"] * 1e3,
             "note": ("temperature-1 acceptance (one Gumbel-max draw per visited node, "

@@ -2,7 +2,8 @@
  * libjtree — one decode step of causal parallel tree drafting (JetSpec) on a
  * GB300 (sm_103a): per-depth top-W candidates, best-first tree expansion,
  * the tree-causal mask, tree attention for the verification pass, greedy
- * acceptance, and the commit of the accepted path's K/V into the prefix cache.
+ * acceptance, the commit of the accepted path's K/V into the prefix cache,
+ * and the draft LM head fused with the top-W selection.
  *
  * Sources (page title, site, section):
  *   [PL] "JetSpec: Breaking the Scaling Ceiling of Speculative Decoding with
@@ -382,6 +383,32 @@ typedef struct {
 } jt_commit_args;
 
 JT_API jt_status jt_tree_commit_kv(const jt_commit_args* args, const jt_exec* exec);
+
+/* ------------------------------------------------------------------------
+ * jt_lmhead_topw — draft logits through the LM head, reduced to top-W.
+ * [PL] App. E "Training and evaluation details": the draft model reuses the
+ * frozen target LM head, so depth d's draft logits are its hidden state times
+ * the LM-head matrix; [PL] App. E "Drafting": the proposer keeps the top-k
+ * tokens and log-probs per position. This call computes
+ *   logits[r][v] = sum_k hidden[r][k] * w_lm[v][k]   (bf16 x bf16, fp32 sums)
+ * and returns exactly what jt_topw (or jt_topw_entropy) returns for those
+ * logits, without writing them to memory.
+ *
+ *   hidden   bf16 [rows][d]        (rows = batch * n_depth draft positions)
+ *   w_lm     bf16 [vocab][d]       (the LM-head weight, row per token)
+ *   tok      int32 [rows][W], logp fp32 [rows][W]   (as jt_topw)
+ *   entropy  fp32 [rows] or NULL   (as jt_topw_entropy)
+ * The logits are fp32 sums of exact bf16 products in the tensor cores'
+ * order, so they differ from an exact dot product by rounding; top-W indices
+ * agree with exact logits except between candidates closer than that.
+ * Limits: d % 64 == 0, 1 <= W <= min(32, vocab). Workspace:
+ * jt_lmhead_topw_workspace_bytes (one small partial per row and 512-token
+ * slice of the vocabulary). No device-side data checks apply.
+ * ------------------------------------------------------------------------ */
+JT_API size_t jt_lmhead_topw_workspace_bytes(int rows, int d, int vocab, int W);
+JT_API jt_status jt_lmhead_topw(const void* hidden, const void* w_lm, int rows, int d, int vocab,
+                                int W, int32_t* tok, float* logp, float* entropy,
+                                const jt_exec* exec);
 
 #ifdef __cplusplus
 }

@@ -226,6 +226,29 @@ jt_status jt_tree_commit_kv(const jt_commit_args* a, const jt_exec* exec) {
   return from_cuda(launch_tree_commit(c, *a));
 }
 
+size_t jt_lmhead_topw_workspace_bytes(int rows, int d, int vocab, int W) {
+  if (rows < 0 || d < 64 || vocab < 1 || W < 1 || W > kMaxW || W > vocab) return 0;
+  return lmhead_workspace_bytes(rows, vocab, W);
+}
+
+jt_status jt_lmhead_topw(const void* hidden, const void* w_lm, int rows, int d, int vocab, int W,
+                         int32_t* tok, float* logp, float* entropy, const jt_exec* exec) {
+  if (rows < 0 || d < 64 || vocab < 1 || W < 1 || W > kMaxW || W > vocab)
+    return JT_ERR_INVALID_ARG;
+  if (d % 64 != 0) return JT_ERR_UNSUPPORTED;
+  if ((long)rows * ((vocab + 511) / 512) > 0x7FFFFFFFL / 64) return JT_ERR_UNSUPPORTED;
+  if (rows > 0 && (!hidden || !w_lm || !tok || !logp)) return JT_ERR_INVALID_ARG;
+  const void* ptrs[] = {hidden, w_lm, tok, logp, entropy};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return JT_ERR_INVALID_ARG;
+  Ctx c;
+  jt_status st = make_ctx(exec, &c);
+  if (st != JT_OK) return st;
+  st = need_workspace(c, lmhead_workspace_bytes(rows, vocab, W));
+  if (st != JT_OK) return st;
+  return from_cuda(launch_lmhead_topw(c, hidden, w_lm, rows, d, vocab, W, tok, logp, entropy));
+}
+
 size_t jt_tree_accept_workspace_bytes(int batch, int B, int n_depth, int vocab) {
   if (batch < 0 || B < 1 || B > kMaxB || n_depth < 1 || n_depth > kMaxDepth || vocab < 1) return 0;
   return accept_workspace_bytes(batch, B, n_depth, vocab);

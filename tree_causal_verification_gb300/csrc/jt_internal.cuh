@@ -90,6 +90,9 @@ cudaError_t launch_tree_accept(const Ctx&, const float* target, const int32_t* p
                                int32_t* acc_nodes, int32_t* bonus, bool sampled = false,
                                float inv_t = 1.0f, uint64_t seed = 0);
 cudaError_t launch_tree_commit(const Ctx&, const jt_commit_args& a);
+size_t lmhead_workspace_bytes(int rows, int vocab, int W);
+cudaError_t launch_lmhead_topw(const Ctx&, const void* hidden, const void* w_lm, int rows, int d,
+                               int vocab, int W, int32_t* tok, float* logp, float* entropy);
 size_t attn_workspace_bytes(const jt_attn_args& a, int num_sms);
 cudaError_t launch_tree_attn(const Ctx&, const jt_attn_args& a);
 

@@ -35,7 +35,7 @@ EXPORTED = ["jt_status_str", "jt_read_device_error", "jt_topw_workspace_bytes", 
             "jt_tree_expand", "jt_tree_mask", "jt_tree_attn_workspace_bytes", "jt_tree_attn",
             "jt_tree_accept_workspace_bytes", "jt_tree_accept", "jt_tree_accept_noalloc",
             "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored",
-            "jt_tree_accept_sampled"]
+            "jt_tree_accept_sampled", "jt_lmhead_topw_workspace_bytes", "jt_lmhead_topw"]
 JT_SCORE_LOGP, JT_SCORE_HYBRID, JT_SCORE_ENTROPY = 0, 1, 2
 
 
@@ -115,10 +115,14 @@ def load(path: str = LIB_PATH):
                                                    _c_int, ctypes.c_float, ctypes.c_uint64, _vp,
                                                    _vp, _vp, _vp, _pexec]
             lib.jt_tree_commit_kv.argtypes = [ctypes.POINTER(jt_commit_args), _pexec]
+            lib.jt_lmhead_topw_workspace_bytes.restype = _c_size
+            lib.jt_lmhead_topw_workspace_bytes.argtypes = [_c_int] * 4
+            lib.jt_lmhead_topw.argtypes = [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
+                                           _pexec]
             for name in ("jt_read_device_error", "jt_topw", "jt_tree_expand", "jt_tree_mask",
                          "jt_tree_attn", "jt_tree_accept", "jt_tree_accept_noalloc",
                          "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored",
-                         "jt_tree_accept_sampled"):
+                         "jt_tree_accept_sampled", "jt_lmhead_topw"):
                 getattr(lib, name).restype = _c_int
             _lib = lib
     return _lib
@@ -416,3 +420,28 @@ def jt_tree_commit_kv(k_tree, v_tree, k_cache, v_cache, prefix_len, acc_len, acc
     c = _exec(exec).c()
     _check(load().jt_tree_commit_kv(ctypes.byref(args), ctypes.byref(c)), "jt_tree_commit_kv")
     return new_prefix_len
+
+
+def jt_lmhead_topw(hidden, w_lm, W, tok=None, logp=None, entropy=None, with_entropy=False,
+                   exec=None):
+    """Top-W of softmax(hidden @ w_lm^T) per row without materialising the
+    logits: hidden bf16 [rows][d], w_lm bf16 [vocab][d] -> (tok, logp[, entropy])."""
+    rows, d = hidden.shape
+    V = w_lm.shape[0]
+    dev = hidden.device
+    _need(hidden, torch.bfloat16, (rows, d), "hidden")
+    _need(w_lm, torch.bfloat16, (V, d), "w_lm")
+    tok = torch.empty((rows, W), dtype=torch.int32, device=dev) if tok is None else tok
+    logp = torch.empty((rows, W), dtype=torch.float32, device=dev) if logp is None else logp
+    _need(tok, torch.int32, (rows, W), "tok")
+    _need(logp, torch.float32, (rows, W), "logp")
+    if with_entropy and entropy is None:
+        entropy = torch.empty((rows,), dtype=torch.float32, device=dev)
+    if entropy is not None:
+        _need(entropy, torch.float32, (rows,), "entropy")
+    lib = load()
+    ex = _exec(exec).reserve(lib.jt_lmhead_topw_workspace_bytes(rows, d, V, W))
+    c = ex.c()
+    _check(lib.jt_lmhead_topw(_ptr(hidden), _ptr(w_lm), rows, d, V, W, _ptr(tok), _ptr(logp),
+                              _ptr(entropy), ctypes.byref(c)), "jt_lmhead_topw")
+    return (tok, logp) if entropy is None else (tok, logp, entropy)
