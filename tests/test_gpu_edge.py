@@ -126,9 +126,11 @@ def test_attention_random(batch, B, n_list, hq, hkv, D, lens, paged):
     ref = oracle.tree_attn(q, kt, vt, kc, vc, lens_np, n, mask, hq=hq, hkv=hkv, block_table=bt)
     d = lambda t: t.to(DEV)
     ex = jtree.Exec(DEV)
-    out = jtree.jt_tree_attn(d(q), d(kt), d(vt), d(kc), d(vc), d(torch.from_numpy(lens_np)),
-                             d(torch.from_numpy(n)), d(torch.from_numpy(mask.view(np.int32))),
-                             block_table=None if bt is None else d(torch.from_numpy(bt)), exec=ex)
+    # NaN-filled: a row the kernels never write fails the comparison.
+    out = torch.full((batch, B, hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    jtree.jt_tree_attn(d(q), d(kt), d(vt), d(kc), d(vc), d(torch.from_numpy(lens_np)),
+                       d(torch.from_numpy(n)), d(torch.from_numpy(mask.view(np.int32))), out=out,
+                       block_table=None if bt is None else d(torch.from_numpy(bt)), exec=ex)
     assert ex.read_error() == 0
     check_attn(out.float().cpu().numpy(), ref)
 
@@ -242,9 +244,10 @@ def test_attention_balanced_schedule(batch, hq, hkv, B, paged, Lmax):
         kc, vc = bf16((batch, Lmax, hkv, D), g), bf16((batch, Lmax, hkv, D), g)
     d = lambda t: t.to(DEV)
     ex = jtree.Exec(DEV)
-    out = jtree.jt_tree_attn(d(q), d(kt), d(vt), d(kc), d(vc), d(torch.from_numpy(lens)),
-                             d(torch.from_numpy(n)), d(torch.from_numpy(mask.view(np.int32))),
-                             block_table=None if bt is None else d(torch.from_numpy(bt)), exec=ex)
+    out = torch.full((batch, B, hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    jtree.jt_tree_attn(d(q), d(kt), d(vt), d(kc), d(vc), d(torch.from_numpy(lens)),
+                       d(torch.from_numpy(n)), d(torch.from_numpy(mask.view(np.int32))), out=out,
+                       block_table=None if bt is None else d(torch.from_numpy(bt)), exec=ex)
     assert ex.read_error() == 0
     rows = [(b, v, h) for b in (0, 1, 2) for v in range(B) for h in range(hq)]
     rows += [(int(b), int(v), int(h)) for b, v, h in

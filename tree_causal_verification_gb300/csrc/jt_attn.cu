@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     for (int i = tid; i < units; i += kPlanThreads) p.nparts[i] = 0;
 }
 
-template <int D, bool BAL>
+template <int D, bool BAL, bool KSPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mkc,
                     const __grid_constant__ CUtensorMap mvc, const __grid_constant__ CUtensorMap mkt,
@@ -410,6 +410,14 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   if (warp == kWarpMMA) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
+  }
+  if (lane == 0 && warp == kWarpTMA) {   // the maps live in parameter space
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mkc);
+    tma_prefetch_desc(&mkt);
+  } else if (lane == 0 && warp == kWarpTMAV) {
+    tma_prefetch_desc(&mvc);
+    tma_prefetch_desc(&mvt);
   }
 
   grid_dependency_sync();
@@ -504,16 +512,25 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     return t < p_tiles ? min(kTile, L - t * kTile) : min(kTile, n - (t - p_tiles) * kTile);
   };
 
+  // Key split: when tile B holds no live node, both softmax warpgroups serve
+  // tile A's rows, warpgroup G taking the key tiles jt = G, G + 2, ... into
+  // its own S/P and O columns (S_G = Q_A K^T), so that the S MMA and the
+  // softmax of one key tile overlap those of the next; their two (m, l, O)
+  // states are merged in the epilogue.
+  const bool ks = KSPLIT && !twoB && T >= 2;
   // Softmax state, read by the common epilogue.
   float m_run = -INFINITY, l_run = 0.0f;
-  const int X = warp >> 2;
+  const int G = warp >> 2;                  // TMEM column group (S/P and O)
+  const int X = ks ? 0 : G;                 // M tile of this thread's row
   const int r = tid & 127;
   const int R = X * kTile + r;              // row within the unit's 256
   const int v = v0 + R / g;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t s_col = tmem + lane_base + X * 128;
-  const uint32_t o_col = tmem + lane_base + 256 + X * OSTRIDE;
+  const uint32_t s_col = tmem + lane_base + G * 128;
+  const uint32_t o_col = tmem + lane_base + 256 + G * OSTRIDE;
   const bool tile_live = X == 0 || twoB;
+  const int j_first = ks ? G : 0, j_step = ks ? 2 : 1;
+  const int T_own = ks ? (T - G + 1) / 2 : T;   // key tiles this warpgroup processes
   bool sm_ok = true;
 
   if (warp >= 8) {
@@ -524,17 +541,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     const bool is_v = warp == kWarpTMAV;
     if (lane == 0 && T > 0) {
       if (!is_v) {
-        tma_prefetch_desc(&mq);
-        tma_prefetch_desc(&mkc);
-        tma_prefetch_desc(&mkt);
         mbar_arrive_expect_tx(&bars->q_full, (twoB ? 2 : 1) * QB);
         for (int X2 = 0; X2 < (twoB ? 2 : 1); ++X2)
 #pragma unroll
           for (int ch = 0; ch < CH; ++ch)
             tma_load_4d(sQ(X2) + ch * CHB, &mq, &bars->q_full, ch * 64, kh * g, v0 + X2 * npt, b);
-      } else {
-        tma_prefetch_desc(&mvc);
-        tma_prefetch_desc(&mvt);
       }
       const CUtensorMap* mc = is_v ? &mvc : &mkc;
       const CUtensorMap* mtr = is_v ? &mvt : &mkt;
@@ -584,23 +595,25 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     const uint64_t qd[2] = {sdesc_sw128(smem_u32(sQ(0)), 16, 1024), sdesc_sw128(smem_u32(sQ(1)), 16, 1024)};
     const uint64_t kd[2] = {sdesc_sw128(smem_u32(sK(0)), 16, 1024), sdesc_sw128(smem_u32(sK(1)), 16, 1024)};
     const uint64_t vd[2] = {sdesc_sw128(smem_u32(sV(0)), CHB, 1024), sdesc_sw128(smem_u32(sV(1)), CHB, 1024)};
-    auto issue_s = [&](int X, int st) {
-      const uint64_t q = qd[X], k = kd[st];
-      const uint32_t d = tmem + X * 128;
+    // S of column group Gd from Q tile Xq and K slot st.
+    auto issue_s = [&](int Xq, int st, int Gd) {
+      const uint64_t q = qd[Xq], k = kd[st];
+      const uint32_t d = tmem + Gd * 128;
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         const uint64_t off = (uint64_t)(((kk >> 2) * CHB + (kk & 3) * 32) >> 4);
         mma_bf16_ss(d, q + off, k + off, id_s, kk > 0);
       }
-      mma_commit(&bars->s_full[X]);
+      mma_commit(&bars->s_full[Gd]);
     };
-    auto issue_pv = [&](int X, int jt) {
+    // O_Gd (+)= P_Gd V, V from the slot of key tile jt; `first` starts O.
+    auto issue_pv = [&](int Gd, int jt, bool first) {
       const uint64_t v = vd[jt % kStages];
-      const uint32_t d = tmem + 256 + X * OSTRIDE, a = tmem + X * 128;
+      const uint32_t d = tmem + 256 + Gd * OSTRIDE, a = tmem + Gd * 128;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_bf16_ts(d, a + kk * 8, v + (uint64_t)(kk * (2048 >> 4)), id_o, jt > 0 || kk > 0);
-      mma_commit(&bars->pv_done[X]);
+        mma_bf16_ts(d, a + kk * 8, v + (uint64_t)(kk * (2048 >> 4)), id_o, !first || kk > 0);
+      mma_commit(&bars->pv_done[Gd]);
     };
     // Rows of V past a tile's valid keys that the TMA read from memory may
     // hold anything (NaN included); P is 0 there but 0 * NaN is NaN, so they
@@ -624,22 +637,62 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     };
     bool ok = T > 0 && warp_wait(&bars->q_full, 0) && warp_wait(&bars->k_full[0], 0);
     if (T > 0 && !ok) fail();
-    if (ok) {
+    if (ok && ks) {
+      // Key split, per key tile t (column group t & 1, local index t >> 1):
+      // S(0), S(1), then PV(t), S(t + 2) for t = 0, 1, 2, ...
       tc_fence_after();
       if (lane == 0) {
-        issue_s(0, 0);
-        if (twoB) issue_s(1, 0);
+        issue_s(0, 0, 0);
+        mma_commit(&bars->k_empty[0]);
+      }
+      __syncwarp();
+      if (!warp_wait(&bars->k_full[1], 0)) { fail(); ok = false; }
+      if (ok) {
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(0, 1, 1);
+          mma_commit(&bars->k_empty[1]);
+        }
+        __syncwarp();
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        const int Gt = t & 1, st = t % kStages;
+        if (!warp_wait(&bars->p_full[Gt], (t >> 1) & 1)) { fail(); ok = false; break; }
+        if (!warp_wait(&bars->v_full[st], (t / kStages) & 1)) { fail(); ok = false; break; }
+        zero_v_tail(t);
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(Gt, t, t < 2);
+          mma_commit(&bars->v_empty[st]);
+        }
+        __syncwarp();
+        if (t + 2 < T) {
+          if (!warp_wait(&bars->k_full[st], ((t + 2) / kStages) & 1)) { fail(); ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            issue_s(0, st, Gt);
+            mma_commit(&bars->k_empty[st]);
+          }
+          __syncwarp();
+        }
+      }
+    } else if (ok) {
+      // Tile pair, per key tile jt: PV_A(jt), S_A(jt+1), PV_B(jt), S_B(jt+1).
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0, 0, 0);
+        if (twoB) issue_s(1, 0, 1);
         mma_commit(&bars->k_empty[0]);   // K tile 0 is no longer needed
       }
       __syncwarp();
     }
-    for (int jt = 0; ok && jt < T; ++jt) {
+    for (int jt = 0; ok && !ks && jt < T; ++jt) {
       const int st = jt % kStages;
       if (!warp_wait(&bars->p_full[0], jt & 1)) { fail(); ok = false; break; }
       if (!warp_wait(&bars->v_full[st], (jt / kStages) & 1)) { fail(); ok = false; break; }
       zero_v_tail(jt);
       tc_fence_after();
-      if (lane == 0) issue_pv(0, jt);
+      if (lane == 0) issue_pv(0, jt, jt == 0);
       __syncwarp();
       const bool more = jt + 1 < T;
       const int st1 = (jt + 1) % kStages;
@@ -647,7 +700,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         if (!warp_wait(&bars->k_full[st1], ((jt + 1) / kStages) & 1)) { fail(); ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
-          issue_s(0, st1);
+          issue_s(0, st1, 0);
           if (!twoB) mma_commit(&bars->k_empty[st1]);
         }
         __syncwarp();
@@ -655,13 +708,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       if (twoB) {
         if (!warp_wait(&bars->p_full[1], jt & 1)) { fail(); ok = false; break; }
         tc_fence_after();
-        if (lane == 0) issue_pv(1, jt);
+        if (lane == 0) issue_pv(1, jt, jt == 0);
         __syncwarp();
       }
       if (lane == 0) {
         mma_commit(&bars->v_empty[st]);
         if (twoB && more) {
-          issue_s(1, st1);
+          issue_s(1, st1, 1);
           mma_commit(&bars->k_empty[st1]);
         }
       }
@@ -678,9 +731,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     for (int w = 0; w < kMaxWords; ++w)
       mrow[w] = (row_valid && w < p.words) ? p.mask[((size_t)b * p.B + v) * p.words + w] : 0u;
     const float sl2 = p.scale_log2;
-    for (int jt = 0; jt < T; ++jt) {
+    for (int jt = j_first, it = 0; jt < T; jt += j_step, ++it) {
       const int t = t_begin + jt;
-      if (!warp_wait(&bars->s_full[X], jt & 1)) { fail(); sm_ok = false; break; }
+      if (!warp_wait(&bars->s_full[G], it & 1)) { fail(); sm_ok = false; break; }
       tc_fence_after();
       // Which keys of this tile the row sees: c < lim, and for tree tiles the
       // ancestor bit of key u0 + c.
@@ -736,8 +789,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         l_run *= corr;
         m_run = mnew;
       }
-      if (jt >= 1 && __any_sync(0xFFFFFFFFu, need)) {
-        // PV_X(jt-1) is complete: the commit behind s_full covers it.
+      if (it >= 1 && __any_sync(0xFFFFFFFFu, need)) {
+        // This group's previous P V is complete: the commit behind s_full covers it.
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -768,10 +821,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       l_run += lsum;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[X]);
+      if (lane == 0) mbar_arrive(&bars->p_full[G]);
     }
-    if (sm_ok && T > 0) {
-      if (warp_wait(&bars->pv_done[X], (T - 1) & 1)) tc_fence_after();
+    if (sm_ok && T_own > 0) {
+      if (warp_wait(&bars->pv_done[G], (T_own - 1) & 1)) tc_fence_after();
       else { fail(); sm_ok = false; }
     }
   }
@@ -783,11 +836,58 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   // take registers a softmax warpgroup still needs to grow, and deadlock.
   __syncthreads();
   if (warp >= 8) regs_inc<kRegsLaunch>();
-  const bool have_o = warp < 8 && tile_live && sm_ok && T > 0;
+  const bool have_o = warp < 8 && tile_live && sm_ok && T_own > 0;
   if (!have_o) { m_run = -INFINITY; l_run = 0.0f; }
   // Every live tile has seen its last P V complete, so the tensor pipe and
   // the K/V ring are idle from here on: the merge buffer may overlay them.
   __syncthreads();
+
+  // Key split: the two warpgroups swap (m, l) through the unused Q_B tile and
+  // each merges one half of the head dimension of the same rows:
+  // O = f_0 O_0 + f_1 O_1, l = f_0 l_0 + f_1 l_1, f_G = 2^(m_G - M), M = max_G m_G.
+  // Each group has waited only for its own last P V: the tcgen05 fences
+  // around the barrier order the other group's MMAs before the TMEM loads.
+  float f0 = 1.0f, f1 = 0.0f;
+  if (ks) {
+    float2* ml = reinterpret_cast<float2*>(sQ(1));
+    if (warp < 8) ml[G * kTile + r] = make_float2(m_run, l_run);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp < 8) {
+      const float2 a0 = ml[r], a1 = ml[kTile + r];
+      const float M = fmaxf(a0.x, a1.x);
+      f0 = a0.x == -INFINITY ? 0.0f : ex2(a0.x - M);
+      f1 = a1.x == -INFINITY ? 0.0f : ex2(a1.x - M);
+      l_run = f0 * a0.y + f1 * a1.y;
+      m_run = M;
+    }
+  }
+  // Columns 32c .. 32c + 31 of this row's O (zeros without one); in a key
+  // split both groups' O, merged 16 columns at a time.
+  const uint32_t o0_col = tmem + lane_base + 256;
+  auto load_o = [&](int c, float (&o)[32]) {
+    if (ks) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float a[16], bb[16];
+        tmem_ld16(o0_col + c * 32 + h * 16, a);
+        tmem_ld16(o0_col + OSTRIDE + c * 32 + h * 16, bb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          o[h * 16 + i] = (f0 != 0.0f ? a[i] * f0 : 0.0f) + (f1 != 0.0f ? bb[i] * f1 : 0.0f);
+      }
+    } else if (have_o) {
+      tmem_ld32(o_col + c * 32, o);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+    }
+  };
+  // 32-column chunks of O this thread writes (a key split halves them).
+  const int c_lo = ks ? G * (D / 64) : 0, c_hi = ks ? c_lo + D / 64 : D / 32;
 
   // ---- output (S == 1) or publish partials (S > 1); both read O from TMEM ----
   const int unit_e = BAL ? ld_shared_volatile(&bars->unit) : unit;
@@ -815,15 +915,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         const int slot = (R % sig) * (2 * kTile / sig) + R / sig;
         float4* po = reinterpret_cast<float4*>(part);
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = c_lo; c < c_hi; ++c) {
           float o[32];
-          if (have_o) {
-            tmem_ld32(o_col + c * 32, o);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0.0f;
-          }
+          load_o(c, o);
           if (live) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
@@ -831,7 +925,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                      make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
           }
         }
-        if (live) {
+        if (live && (!ks || G == 0)) {
           __stcg(part + 2 * kTile * D + slot, m_run);
           __stcg(part + 2 * kTile * D + 2 * kTile + slot, l_run);
         }
@@ -839,15 +933,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     } else {
       uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b_e * p.B + v) * p.hq + kh_e * g + j) * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = c_lo; c < c_hi; ++c) {
         float o[32];
-        if (have_o) {
-          tmem_ld32(o_col + c * 32, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0.0f;
-        }
+        load_o(c, o);
         if (write_row) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -857,6 +945,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                                         pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
         }
       }
+    }
+  }
+
+  // Key split with direct output: tile B's rows hold no live node; the
+  // third warpgroup writes the zeros of those inside the budget (the split-KV
+  // merges zero every unused row themselves).
+  if (ks && split_e == 1 && warp >= 8) {
+    const int Rb = kTile + (tid - 256);
+    const int vb = v0_e + Rb / g;
+    if (vb < p.B) {
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b_e * p.B + vb) * p.hq + kh_e * g + Rb % g) * D);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
     }
   }
 
@@ -960,7 +1061,9 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   const size_t smem = smem_bytes<D>();
   const int units = a.batch * a.hkv * p.n_mpairs;
   const Schedule sc = pick_schedule(a, p, c.num_sms);
-  auto kern = sc.balanced ? tree_attn_tc_kernel<D, true> : tree_attn_tc_kernel<D, false>;
+  // Residency queries use the plain variant (both variants have the same
+  // shared memory and threads).
+  auto kern = sc.balanced ? tree_attn_tc_kernel<D, true, false> : tree_attn_tc_kernel<D, false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
 
@@ -1014,6 +1117,15 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
     S = cand;
   }
   p.S = S;
+  // Key split variant: no unit can have a live tile B (the budget fits one M
+  // tile, B <= 128 / g) and some CTA gets two key tiles or more.
+  const int tiles_max = (p.Lbound + kTile - 1) / kTile + (a.B + kTile - 1) / kTile;
+  const int cta_tiles = sc.balanced ? sc.chunk_tiles : (tiles_max + S - 1) / S;
+  if (a.B <= p.npt && cta_tiles >= 2) {
+    kern = sc.balanced ? tree_attn_tc_kernel<D, true, true> : tree_attn_tc_kernel<D, false, true>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
 
   CUtensorMap mq, mkc, mvc, mkt, mvt;
   const uint64_t D64 = D;
