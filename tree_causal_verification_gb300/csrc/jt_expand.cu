@@ -14,11 +14,13 @@
 // A pop is two warp reductions: __reduce_max_sync over an order-preserving
 // uint32 key of the score, then __reduce_min_sync over the ids holding that
 // key (ties -> lower id, as the heap order requires). The W children of a
-// pop are created by W lanes at once; each is handed to its owner lane by a
-// shuffle. Scores are binary32 sums (__fadd_rn), the same adds as the
-// definition. The sequence's N x W candidates are staged in shared memory
-// first, so no pop waits on a global load (the depth that selects the next
-// candidate row is only known once the pop is done).
+// pop are created at once, each by the lane that will hold it; the popped
+// node's score is recovered from its key and its depth comes by one shuffle
+// from the lane that held it, so a pop touches no memory besides the
+// candidate row of the next depth. Scores are binary32 sums (__fadd_rn), the
+// same adds as the definition. The sequence's N x W candidates are staged in
+// shared memory first, so no pop waits on a global load (the depth that
+// selects the next candidate row is only known once the pop is done).
 //
 // Score modes (paperlayer.ai App. C "Tree-Drafting Algorithm Ablation" and
 // App. E "Drafting": cumulative log-prob, entropy-guided and hybrid scores).
@@ -34,6 +36,11 @@ namespace {
 
 constexpr int kWarpsPerBlock = 4;
 
+// Inverse of order_key for the keys of real values (never 0 here).
+__device__ __forceinline__ float key_score(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 template <int SLOTS>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ logp,
@@ -41,8 +48,6 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
                    int N, int W, int B, int32_t* __restrict__ parent_o,
                    int32_t* __restrict__ token_o, int32_t* __restrict__ depth_o,
                    float* __restrict__ score_o, int32_t* __restrict__ n_nodes_o) {
-  __shared__ float score_s[kWarpsPerBlock][kMaxB];
-  __shared__ uint8_t depth_s[kWarpsPerBlock][kMaxB];
   extern __shared__ int32_t cand_s[];   // per warp: N*W tokens then N*W score increments
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -69,16 +74,16 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
   int32_t* tko = token_o + (size_t)b * B;
   int32_t* dpo = depth_o + (size_t)b * B;
   float* sco = score_o + (size_t)b * B;
-  float* scs = score_s[warp];
-  uint8_t* dep = depth_s[warp];
 
-  // Frontier keys of this lane's slots (node (slot << 5) | lane); 0 = empty.
-  // best_key / best_slot cache the lane's own best (highest key, lowest slot).
+  // Frontier keys and depths of this lane's slots (node (slot << 5) | lane);
+  // key 0 = empty. best_* cache the lane's own best (highest key, lowest
+  // slot) and its depth.
   uint32_t fk[SLOTS];
+  int fd[SLOTS];
 #pragma unroll
-  for (int k = 0; k < SLOTS; ++k) fk[k] = 0u;
+  for (int k = 0; k < SLOTS; ++k) { fk[k] = 0u; fd[k] = 0; }
   uint32_t best_key = 0u;
-  int best_slot = 0;
+  int best_slot = 0, best_depth = 0;
 
   int count = 0;
   int cur = -1;          // the node being expanded; the root first
@@ -87,41 +92,41 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
   while (true) {
     const int d = cur_d + 1;               // depth of the children
     const int nc = min(W, B - count);
-    float csc = 0.0f;
-    if (lane < nc) {                       // lane r creates child r
-      const int v = count + lane;
-      const int t = tk[(d - 1) * W + lane];
-      csc = __fadd_rn(cur_s, lp[(d - 1) * W + lane]);
+    // Child r of this pop is node count + r, owned (and created) by lane
+    // (count + r) & 31.
+    const int r = (lane - count) & 31;
+    if (r < nc) {
+      const int v = count + r;
+      const float csc = __fadd_rn(cur_s, lp[(d - 1) * W + r]);
       par[v] = cur;
-      tko[v] = t;
+      tko[v] = tk[(d - 1) * W + r];
       dpo[v] = d;
       sco[v] = csc;
-      scs[v] = csc;
-      dep[v] = (uint8_t)d;
-    }
-    // Owner lane of child v = count + r is lane v & 31, i.e. r = (lane - count) & 31.
-    const int r = (lane - count) & 31;
-    const float sv = __shfl_sync(kFull, csc, r);
-    if (d < N && r < nc) {
-      const int slot = (count + r) >> 5;
-      const uint32_t key = order_key(sv);
+      if (d < N) {
+        const int slot = v >> 5;
+        const uint32_t key = order_key(csc);
 #pragma unroll
-      for (int k = 0; k < SLOTS; ++k)
-        if (k == slot) fk[k] = key;
-      // A new node has a higher id than every node of its lane, so it
-      // displaces the cached best only with a strictly higher key.
-      if (key > best_key) { best_key = key; best_slot = slot; }
+        for (int k = 0; k < SLOTS; ++k)
+          if (k == slot) { fk[k] = key; fd[k] = d; }
+        // A new node has a higher id than every node of its lane, so it
+        // displaces the cached best only with a strictly higher key.
+        if (key > best_key) { best_key = key; best_slot = slot; best_depth = d; }
+      }
     }
     count += nc;
-    __syncwarp();
     if (count >= B) break;
 
-    // Pop: best (key desc, id asc) over the frontier.
+    // Pop: best (key desc, id asc) over the frontier. The popped score is
+    // the key's value (order_key is a bijection on the scores, which are
+    // never -0: they start at +0 and a round-to-nearest sum is -0 only
+    // when both terms are), and its depth comes from the owner lane.
     const uint32_t top = __reduce_max_sync(kFull, best_key);
     if (top == 0) break;  // nothing expandable
     const uint32_t id = __reduce_min_sync(
         kFull, best_key == top ? (uint32_t)((best_slot << 5) | lane) : 0xFFFFFFFFu);
-    if ((int)(id & 31u) == lane) {
+    const int owner = (int)(id & 31u);
+    cur_d = __shfl_sync(kFull, best_depth, owner);
+    if (lane == owner) {
       // The owner drops the popped slot and rescans its remaining slots.
       const int ps = (int)(id >> 5);
 #pragma unroll
@@ -129,13 +134,13 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
         if (k == ps) fk[k] = 0u;
       best_key = 0u;
       best_slot = 0;
+      best_depth = 0;
 #pragma unroll
       for (int k = SLOTS - 1; k >= 0; --k)
-        if (fk[k] >= best_key && fk[k] != 0u) { best_key = fk[k]; best_slot = k; }
+        if (fk[k] >= best_key && fk[k] != 0u) { best_key = fk[k]; best_slot = k; best_depth = fd[k]; }
     }
     cur = (int)id;
-    cur_s = scs[cur];
-    cur_d = dep[cur];
+    cur_s = key_score(top);
   }
   for (int v = count + lane; v < B; v += 32) {
     par[v] = -1;
