@@ -435,7 +435,11 @@ __device__ __forceinline__ bool cluster_reduce(ScanPartial<K>* mine, int S, TopK
     if (LSE) lse.warp_reduce();
     holder = (lane == 0);
   }
-  cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
+  // Keep every CTA's shared memory alive until rank 0 has read it. Rank 0
+  // has consumed every value it loaded before it arrives, so the barrier
+  // needs no memory ordering: a relaxed arrive skips the release fence.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   return holder;
 }
 
