@@ -764,22 +764,18 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       }
       tmem_wait_ld();
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (full) {
-#pragma unroll
-        for (int i = 0; i < kTile; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
-      } else {
+      if (!full) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int rem = lim - c * 32;
           const uint32_t lim_bits = rem >= 32 ? 0xFFFFFFFFu : rem <= 0 ? 0u : (1u << rem) - 1u;
           const uint32_t vw = word_of(c) & lim_bits;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[c * 32 + i] = ((vw >> i) & 1u) ? x[c * 32 + i] : -INFINITY;
-            m4[i & 3] = fmaxf(m4[i & 3], x[c * 32 + i]);
-          }
+          for (int i = 0; i < 32; ++i) x[c * 32 + i] = ((vw >> i) & 1u) ? x[c * 32 + i] : -INFINITY;
         }
       }
+#pragma unroll
+      for (int i = 0; i < kTile; i += 2) m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], x[i], x[i + 1]);
       const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
       const float mnew = fmaxf(m_run, tmax);
       const bool need = mnew > m_run + kRescaleLog2;
@@ -801,22 +797,29 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
           tmem_st32(o_col + c * 32, o);
         }
       }
-      // P = 2^(s sl2 - m) as bf16 pairs over the S columns (all already read).
+      // P = 2^(s sl2 - m) as bf16 pairs over the S columns (all already read);
+      // the exponent argument and the row sum go two columns per packed
+      // fp32x2 instruction.
       const float muse = (m_run == -INFINITY) ? 0.0f : m_run;
-      float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(-muse, -muse);
+      uint64_t ls2[2] = {f32x2(0.0f, 0.0f), f32x2(0.0f, 0.0f)};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(x[c * 32 + 2 * i], sl2, -muse));
-          const float p1 = ex2(fmaf(x[c * 32 + 2 * i + 1], sl2, -muse));
-          ls[i & 3] += p0 + p1;
+          float y0, y1;
+          f32x2_split(ffma2(f32x2(x[c * 32 + 2 * i], x[c * 32 + 2 * i + 1]), sl2x2, negm2), y0, y1);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
           pk[i] = pack_bf16(p0, p1);
         }
         tmem_st16(s_col + c * 16, pk);
       }
-      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      float l0, l1, l2, l3;
+      f32x2_split(ls2[0], l0, l1);
+      f32x2_split(ls2[1], l2, l3);
+      const float lsum = (l0 + l1) + (l2 + l3);
       tmem_wait_st();
       l_run += lsum;
       tc_fence_before();
