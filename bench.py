@@ -55,7 +55,7 @@ CALL_SOURCES = {
     "jt_topw": ["jt_topw.cu", "jt_rowscan.cuh"],
     "jt_tree_expand": ["jt_expand.cu"],
     "jt_tree_mask": ["jt_mask.cu"],
-    "jt_tree_attn": ["jt_attn.cu"],
+    "jt_tree_attn": ["jt_attn.cu", "jt_sm100.cuh"],
     "jt_tree_accept": ["jt_accept.cu", "jt_rowscan.cuh"],
 }
 
