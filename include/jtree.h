@@ -61,7 +61,7 @@ typedef struct CUstream_st* jt_stream_t;
 typedef enum {
   JT_OK = 0,
   JT_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, misaligned pointer */
-  JT_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. head_dim 96) */
+  JT_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement (e.g. head_dim 96) */
   JT_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
   JT_ERR_DEVICE_DATA = 4,   /* jt_read_device_error found a device-side flag set */
   JT_ERR_TIMEOUT = 5,       /* a bounded device-side wait expired (flag JT_DEVERR_TIMEOUT) */

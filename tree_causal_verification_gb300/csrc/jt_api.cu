@@ -55,7 +55,7 @@ const char* jt_status_str(jt_status s) {
   switch (s) {
     case JT_OK: return "JT_OK";
     case JT_ERR_INVALID_ARG: return "JT_ERR_INVALID_ARG: bad argument (null, size or alignment)";
-    case JT_ERR_UNSUPPORTED: return "JT_ERR_UNSUPPORTED: request outside what this build implements";
+    case JT_ERR_UNSUPPORTED: return "JT_ERR_UNSUPPORTED: request outside what the library implements";
     case JT_ERR_CUDA: return "JT_ERR_CUDA: a CUDA call or kernel launch failed";
     case JT_ERR_DEVICE_DATA: return "JT_ERR_DEVICE_DATA: a device-side data check failed";
     case JT_ERR_TIMEOUT: return "JT_ERR_TIMEOUT: a bounded device-side wait expired";
