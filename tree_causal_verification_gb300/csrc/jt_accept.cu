@@ -50,7 +50,7 @@ accept_argmax_kernel(const float* __restrict__ target, const int32_t* __restrict
     scan_segment<1, false, false, GumbelKeys>(target + (size_t)row * V, lo, hi, top, lse,
                                               GumbelKeys{seed, (uint64_t)row << 32, inv_t});
   else
-    scan_segment<1, false>(target + (size_t)row * V, lo, hi, top, lse);
+    scan_segment<1, false, false, IdentityXf, true>(target + (size_t)row * V, lo, hi, top, lse);
   block_reduce<1, false>(top, lse, &part, warp_parts);
   if (cluster_reduce<1, false>(&part, S, top, lse)) am[row] = top.i[0];
 }

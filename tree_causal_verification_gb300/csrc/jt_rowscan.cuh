@@ -238,7 +238,10 @@ __device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0
 // Streams float4s [lo4, hi4) of `row` into per-thread state: full batches
 // without bounds checks, ping-ponging two register buffers so that one batch
 // is in flight while the other is processed, then a checked tail.
-template <int K, bool LSE, bool ENT = false, class Xf = IdentityXf>
+// EARLY_TAIL: a segment of at most two full batches issues its tail's loads
+// together with them (one round trip to memory instead of two); measured to
+// pay off for the plain argmax only, the log-sum-exp and keyed scans lose.
+template <int K, bool LSE, bool ENT = false, class Xf = IdentityXf, bool EARLY_TAIL = false>
 __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int lo4, int hi4,
                                              TopK<K>& top, Lse& lse, const Xf& xf = Xf()) {
   const float4* r4 = reinterpret_cast<const float4*>(row);
@@ -255,9 +258,22 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u) a[u] = ld_stream(r4 + base + tid + u * kScanThreads);
   }
+  const bool early_tail = EARLY_TAIL && full_end - lo4 <= 2 * STEP && full_end < hi4;
+  float4 tl[kScanBatch];
+  if (early_tail) {
+    if (base + STEP < full_end) {
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) b[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
+    }
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) {
+      const int j = full_end + tid + u * kScanThreads;
+      tl[u] = j < hi4 ? ld_stream(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+  }
   while (base < full_end) {
     const bool nb = base + STEP < full_end;
-    if (nb) {
+    if (nb && !(early_tail && base == lo4)) {   // the early tail loaded batch 1 already
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) b[u] = ld_stream(r4 + base + STEP + tid + u * kScanThreads);
     }
@@ -284,7 +300,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u) {
       const int j = full_end + tid + u * kScanThreads;
-      a[u] = j < hi4 ? xf(ld_stream(r4 + j), j) : ninf;
+      a[u] = j < hi4 ? xf(early_tail ? tl[u] : ld_stream(r4 + j), j) : ninf;
     }
     if (full_end + tid < hi4) {
       // Lanes whose whole batch is padding skip it (their padding would
