@@ -62,7 +62,9 @@ def test_topw_ties_and_neg_inf():
 
 @pytest.mark.parametrize("batch,N,W,B", [(1, 4, 2, 16), (5, 16, 4, 256), (3, 64, 1, 64),
                                          (9, 8, 4, 64), (2, 16, 32, 255), (4, 3, 3, 33),
-                                         (1, 1, 8, 5), (6, 2, 2, 31), (2, 64, 2, 256)])
+                                         (1, 1, 8, 5), (6, 2, 2, 31), (2, 64, 2, 256),
+                                         # width 1: chains cut by the budget or by the depth
+                                         (2, 20, 1, 7), (3, 5, 1, 40), (1, 1, 1, 1)])
 def test_expand_and_mask_random(batch, N, W, B):
     rng = np.random.default_rng(batch * 1000 + N * 10 + W + B)
     tok = rng.integers(0, 50000, (batch, N, W)).astype(np.int32)

@@ -57,7 +57,7 @@ def test_topw_entropy_closed_forms():
 
 @pytest.mark.parametrize("mode,alpha", [(0, 0.0), (1, 0.0), (1, 0.25), (1, 2.0), (2, 0.0)])
 @pytest.mark.parametrize("batch,N,W,B", [(4, 4, 2, 16), (3, 16, 4, 256), (5, 8, 4, 64),
-                                         (2, 16, 1, 16), (9, 64, 2, 200)])
+                                         (2, 16, 1, 16), (9, 64, 2, 200), (2, 12, 1, 9)])
 def test_expand_scored(mode, alpha, batch, N, W, B):
     rng = np.random.default_rng(N * W + B + mode)
     tok = np.stack([np.stack([rng.choice(5000, W, replace=False) for _ in range(N)])

@@ -75,6 +75,30 @@ tree_expand_kernel(const int32_t* __restrict__ tok, const float* __restrict__ lo
   int32_t* dpo = depth_o + (size_t)b * B;
   float* sco = score_o + (size_t)b * B;
 
+  if (W == 1) {
+    // Width 1: every pop finds exactly one frontier node, the last child, so
+    // the expansion is the chain of min(B, N) nodes, node v = child of
+    // v - 1 at depth v + 1 with the rank-0 candidate of that depth. Its
+    // scores are the same binary32 sums, in the same order, from +0.
+    const int n = min(B, N);
+    for (int v = lane; v < B; v += 32) {
+      const bool live = v < n;
+      par[v] = live ? v - 1 : -1;
+      tko[v] = live ? tk[v] : -1;
+      dpo[v] = live ? v + 1 : 0;
+      if (!live) sco[v] = 0.0f;
+    }
+    if (lane == 0) {
+      float sc = 0.0f;
+      for (int v = 0; v < n; ++v) {
+        sc = __fadd_rn(sc, lp[v]);
+        sco[v] = sc;
+      }
+      n_nodes_o[b] = n;
+    }
+    return;
+  }
+
   // Frontier keys and depths of this lane's slots (node (slot << 5) | lane);
   // key 0 = empty. best_* cache the lane's own best (highest key, lowest
   // slot) and its depth.
