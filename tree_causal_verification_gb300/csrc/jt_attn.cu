@@ -44,6 +44,13 @@
 //              certifies that PV_X(j) has finished with P_X / O_X.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D),
 // O_B [256+D', ...) with D' = 128 for D = 128 (384..511).
+// Key-split instance (KSPLIT, chosen when the budget fits one M tile): tile
+// B has no live node, so warpgroup G (0 or 1) takes the key tiles G, G+2, ...
+// of tile A's rows into the S_G / O_G columns, the MMA order per key tile t
+// being PV_G(t), S_G(t+2); the two (m, l, O) states merge in the epilogue.
+// In the softmax the exponent argument and the row sum run two columns per
+// packed fp32x2 instruction and the row max uses the three-input max: the
+// softmax warps are bound by instruction issue, not by the exponential unit.
 // Every mbarrier wait is bounded; on expiry the CTA raises JT_DEVERR_TIMEOUT,
 // drains its outstanding MMAs, frees TMEM and finishes.
 #include <cooperative_groups.h>
