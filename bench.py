@@ -3,8 +3,12 @@
 
 A step is the whole path through libjtree's C ABI on inputs resident in HBM:
 top-W per depth -> best-first expansion -> tree mask -> tree attention ->
-greedy acceptance. Default workload: batch 1, prefix 2048, a 16-node chain
-(N=16, W=1), 32/8 heads, head_dim 128, vocabulary 151936 (Qwen3-8B shapes).
+greedy acceptance. The headline workload (default) is the largest one that
+fits one GPU: batch 64, prefixes U[2048, 16384] in 16-token pages, a
+128-node tree (N=16, W=4) per sequence, 32 query / 4 KV heads of 128,
+vocabulary 151936 (MoE-target attention shape). The other four workloads
+(tiny, Qwen3-8B chain, high budget, mid-batch) are measured in the same run
+and reported under "per_config".
 
 Timing: W eager warm-up steps, then EXACTLY K steps captured into one CUDA
 graph and launched once, bracketed by a barrier and a device synchronise on
@@ -12,15 +16,20 @@ both sides, timed by CUDA events recorded on the launching stream at the two
 ends. Each call's average duration comes from a further timed region per
 call: one graph of K launches of that call alone on the same input sets
 (events at its two ends); those feed the roofline figures. Steps rotate
-through enough independent input sets that the inputs exceed the 129 MB L2.
-SM clocks and throttle reasons are sampled through NVML during that region.
+through enough independent input sets that the inputs exceed the 129 MB L2
+(or one set alone exceeds it). SM clocks and throttle reasons are sampled
+through NVML during the timed regions.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (the
 path shards by sequence with no exchange: weak scaling); value = nodes of all
 ranks / the slowest rank's time.
 
---impl reference times the CPU oracle (the plain C++ reference, untuned) on
-the host cores: each step is a one-node sample of the same workload.
+The CPU oracle (the plain C++ reference, untuned) is timed on whole steps:
+every row of a sequence's step (its top-W rows, expansion, mask, every
+(node, head) attention row, acceptance walk), with the rows of a step spread
+over the host's cores (each thread runs the unchanged single-threaded oracle
+on its share). --impl reference times only that oracle, one sequence's whole
+step per timed step.
 
 Prints ONE JSON line (rank 0).
 """
@@ -33,7 +42,6 @@ import json
 import math
 import os
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -44,7 +52,7 @@ if ROOT not in sys.path:
 
 METRIC = "tree nodes verified/sec per step (attn+top-W+accept); % of GB300 HBM/tensor roofline"
 UNIT = "nodes/s"
-DEFAULT_WORKLOAD = "qwen3-8b-chain"
+DEFAULT_WORKLOAD = "moe-paged"
 L2_BYTES = 129e6
 CALLS = ["jt_topw", "jt_tree_expand", "jt_tree_mask", "jt_tree_attn", "jt_tree_accept"]
 # Kernels each call launches (the acceptance call runs an argmax pass and a walk).
@@ -289,137 +297,190 @@ def set_bytes(inp):
 
 
 # --------------------------------------------------------------------------
-# CPU oracle legs.
+# CPU oracle: whole steps on the host cores.
 # --------------------------------------------------------------------------
-def oracle_host_inputs(inp):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleInputs:
+    """Host copies of one input set for the oracle (bf16 tensors as bit
+    patterns). Draft and target rows are copied per sequence, untimed."""
+
+    def __init__(self, w, inp):
+        import numpy as np
+        import torch
+
+        def bits(t):
+            return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+        self.w = w
+        self.q, self.kt, self.vt = bits(inp["q"]), bits(inp["k_tree"]), bits(inp["v_tree"])
+        self.kc, self.vc = bits(inp["k_cache"]), bits(inp["v_cache"])
+        self.prefix = inp["prefix_len"].cpu().numpy()
+        self.bt = None if inp["block_table"] is None else inp["block_table"].cpu().numpy()
+        self._draft, self._target = inp["draft"], inp["target"]
+
+    def rows_of(self, b):
+        """(draft [1][N][V], target [1][B+1][V]) of sequence b, float32 on the host."""
+        return self._draft[b:b + 1].cpu().numpy(), self._target[b:b + 1].cpu().numpy()
+
+
+def oracle_sequence_step(oi, b, rows, pool, threads):
+    """The oracle's whole step for sequence b: its N top-W rows, the
+    expansion, the mask, every (node, head) attention row and the acceptance
+    walk. With threads > 1 the top-W rows and the attention rows are spread
+    over the pool (each task is the unchanged single-threaded oracle on its
+    rows). Returns (nodes, seconds)."""
     import numpy as np
-    h = {}
-    for k, t in inp.items():
-        h[k] = None if t is None else t.cpu()
-    h["draft_np"] = h["draft"].numpy()
-    h["target_np"] = h["target"].numpy()
-    h["prefix_np"] = h["prefix_len"].numpy()
-    h["bt_np"] = None if h["block_table"] is None else h["block_table"].numpy()
-    return h, np
 
-
-def oracle_node_sample(w, h, v, full):
-    """One node's share of a step, by the oracle: its depth's top-W row, the
-    sequence's expansion and mask, the node's attention over every head, and
-    the sequence's acceptance walk. ``full`` = (tok, logp) of sequence 0."""
     import oracle
-    tree = oracle.tree_expand(full[0], full[1], w.B)
-    d = max(int(tree["depth"][0, v]), 1)
-    oracle.topw(h["draft_np"][0:1, d - 1:d], w.W)
+    w = oi.w
+    draft, target = rows
+    paged = oi.bt is not None
+    sl = slice(b, b + 1)
+    t0 = time.perf_counter()
+    if threads > 1:
+        parts = list(pool.map(lambda d: oracle.topw(draft[:, d:d + 1], w.W), range(w.N)))
+        tok = np.concatenate([p[0] for p in parts], axis=1)
+        logp = np.concatenate([p[1] for p in parts], axis=1)
+    else:
+        tok, logp = oracle.topw(draft, w.W)
+    tree = oracle.tree_expand(tok, logp, w.B)
     mask = oracle.tree_mask(tree["parent"], tree["n_nodes"])
-    rows = [(0, v, hh) for hh in range(w.hq)]
-    oracle.tree_attn(h["q"][0:1], h["k_tree"][0:1], h["v_tree"][0:1],
-                     h["k_cache"] if w.paged else h["k_cache"][0:1],
-                     h["v_cache"] if w.paged else h["v_cache"][0:1],
-                     h["prefix_np"][0:1], tree["n_nodes"], mask, hq=w.hq, hkv=w.hkv,
-                     block_table=None if h["bt_np"] is None else h["bt_np"][0:1], rows=rows)
-    oracle.tree_accept(h["target_np"][0:1], tree["parent"], tree["token"], tree["n_nodes"], w.N)
-    return tree
+    n = int(tree["n_nodes"][0])
+    rws = np.array([(0, v, h) for v in range(n) for h in range(w.hq)], np.int32).reshape(-1, 3)
+
+    def attn(r):
+        return oracle.tree_attn(oi.q[sl], oi.kt[sl], oi.vt[sl], oi.kc if paged else oi.kc[sl],
+                                oi.vc if paged else oi.vc[sl], oi.prefix[sl], tree["n_nodes"],
+                                mask, hq=w.hq, hkv=w.hkv, block_table=oi.bt[sl] if paged else None,
+                                rows=r)
+
+    if threads > 1 and len(rws) > 1:
+        list(pool.map(attn, np.array_split(rws, min(len(rws), 4 * threads))))
+    elif len(rws):
+        attn(rws)
+    oracle.tree_accept(target, tree["parent"], tree["token"], tree["n_nodes"], w.N)
+    return n, time.perf_counter() - t0
 
 
-def oracle_leg(w, inp, steps=None, warmup=0, budget_s=12.0):
-    """Times the oracle on one-node samples (rank 0, host cores, 1 thread)."""
+def oracle_timing(w, inp, seqs, threads, budget_s=None, warmup=0):
+    """Times the oracle's whole step for the sequences `seqs`, in order, on
+    `threads` host threads; stops once budget_s seconds of oracle time are
+    spent (at least one sequence). Returns dict(nodes, seconds, seqs)."""
+    import concurrent.futures as cf
+
     import oracle
     oracle.build()
-    h, _ = oracle_host_inputs(inp)
-    full = oracle.topw(h["draft_np"][0:1], w.W)
-    tree = oracle.tree_expand(full[0], full[1], w.B)
-    n0 = int(tree["n_nodes"][0])
-    for i in range(warmup):
-        oracle_node_sample(w, h, i % n0, full)
-    t0 = time.perf_counter()
-    done = 0
-    while True:
-        oracle_node_sample(w, h, done % n0, full)
-        done += 1
-        el = time.perf_counter() - t0
-        if steps is not None and done >= steps:
-            break
-        if steps is None and el >= budget_s:
-            break
-    el = time.perf_counter() - t0
-    return {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} one-node samples of sequence 0 ({w.name}): the node's depth row "
-                      f"top-W (V={w.V}), the sequence's expansion, mask and acceptance walk, and "
-                      f"the node's attention over all {w.hq} heads and "
-                      f"{int(h['prefix_np'][0])}+tree keys; single thread, {el:.1f} s",
-            "seconds": el, "samples": done}
+    oi = OracleInputs(w, inp)
+    nodes, secs, done = 0, 0.0, []
+    with cf.ThreadPoolExecutor(max_workers=threads) as pool:
+        for i in range(warmup):
+            b = seqs[i % len(seqs)]
+            oracle_sequence_step(oi, b, oi.rows_of(b), pool, threads)
+        for b in seqs:
+            n, dt = oracle_sequence_step(oi, b, oi.rows_of(b), pool, threads)
+            nodes += n
+            secs += dt
+            done.append(b)
+            if budget_s is not None and secs >= budget_s:
+                break
+    return {"nodes": nodes, "seconds": secs, "seqs": done}
+
+
+def describe_oracle(w, r, threads, whole):
+    what = ("the whole step (every sequence)" if whole else
+            f"{len(r['seqs'])} of the {w.batch} sequences, each sequence's whole step")
+    return (f"oracle on {what} of {w.name}: top-W of its {w.N} rows (V={w.V}), expansion, mask, "
+            f"attention of every (node, head) row over its prefix and tree keys, acceptance walk; "
+            f"{r['nodes']} nodes in {r['seconds']:.2f} s on {threads} host thread(s)")
 
 
 # --------------------------------------------------------------------------
-# Main.
+# GPU measurement of one workload.
 # --------------------------------------------------------------------------
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", default="jtree", choices=["jtree", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=None)
-    args = ap.parse_args()
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
+def call_fns(w, jtree, inp, bf, ex):
+    return {
+        "jt_topw": lambda: jtree.jt_topw(inp["draft"], w.W, bf.tok, bf.logp, exec=ex),
+        "jt_tree_expand": lambda: jtree.jt_tree_expand(bf.tok, bf.logp, w.B, out=bf.tree, exec=ex),
+        "jt_tree_mask": lambda: jtree.jt_tree_mask(bf.tree["parent"], bf.tree["n_nodes"],
+                                                   bf.mask, exec=ex),
+        "jt_tree_attn": lambda: jtree.jt_tree_attn(
+            inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"], inp["v_cache"],
+            inp["prefix_len"], bf.tree["n_nodes"], bf.mask, out=bf.attn_out,
+            block_table=inp["block_table"], exec=ex),
+        "jt_tree_accept": lambda: jtree.jt_tree_accept(inp["target"], bf.tree["parent"],
+                                                       bf.tree["token"], bf.tree["n_nodes"],
+                                                       w.N, out=bf.acc, exec=ex),
+    }
 
+
+class Timer:
+    """CUDA graphs of K launches with events at their two ends."""
+
+    def __init__(self, rt, stream):
+        self.rt, self.stream = rt, stream
+        self.sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def capture(self, body):
+        import torch
+        events = [ctypes.c_void_p(), ctypes.c_void_p()]
+        for ev in events:
+            _ok(self.rt.cudaEventCreateWithFlags(ctypes.byref(ev), 0), "cudaEventCreateWithFlags")
+        g = Graph(self.rt, self.stream)
+        with torch.cuda.stream(self.stream):
+            with g:
+                _ok(self.rt.cudaEventRecordWithFlags(events[0], self.sptr, 1),
+                    "cudaEventRecordWithFlags")
+                body()
+                _ok(self.rt.cudaEventRecordWithFlags(events[1], self.sptr, 1),
+                    "cudaEventRecordWithFlags")
+        g.upload()
+        return g, events
+
+    def elapsed(self, events):
+        ms = ctypes.c_float(0)
+        _ok(self.rt.cudaEventElapsedTime(ctypes.byref(ms), events[0], events[1]),
+            "cudaEventElapsedTime")
+        return ms.value
+
+    def release(self, g, events):
+        g.close()
+        for ev in events:
+            self.rt.cudaEventDestroy(ev)
+
+    def run(self, body, dev, sampler=None, dist=None):
+        """Captures body (K launches), then times one launch of the graph."""
+        import torch
+        g, ev = self.capture(body)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        if sampler is not None:
+            with sampler:
+                g.launch()
+                self.stream.synchronize()
+        else:
+            g.launch()
+            self.stream.synchronize()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        ms = self.elapsed(ev)
+        nodes = g.kernel_nodes()
+        self.release(g, ev)
+        return ms, nodes
+
+
+def measure(w, K, Wm, dev, stream, timer, ex, seed0=0, dist=None, local=0):
+    """K whole steps (the headline timed region) and K launches of each call
+    alone, on rotating input sets; returns the raw measurements."""
     import torch
-    from tree_causal_verification_gb300 import jtree, synth
-    from tree_causal_verification_gb300.dist import job_throughput, max_over_ranks, rank_world
-
-    rank, world, local = rank_world()
     from tree_causal_verification_gb300.step import StepBuffers, run_step
-
-    w = synth.WORKLOADS[args.workload]
-    wdesc = {"workload": w.name, "batch": w.batch, "prefix": [w.prefix_lo, w.prefix_hi],
-             "B": w.B, "N": w.N, "W": w.W, "hq": w.hq, "hkv": w.hkv, "head_dim": w.D,
-             "vocab": w.V, "paged": w.paged}
-
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        # CPU oracle on the host cores; inputs drawn on the CPU generator.
-        inp, meta = {}, None
-        draft_ext = synth.draft_logits(w, 0, "cpu")
-        kv = synth.kv_inputs(w, 0, "cpu")
-        import oracle
-        oracle.build()
-        tok, logp = oracle.topw(draft_ext[:1, : w.N].contiguous().numpy(), w.W)
-        t1 = oracle.tree_expand(tok, logp, w.B)
-        # Only sequence 0 is sampled; draw its target rows for its tree.
-        w1 = synth.Workload(**{**w.__dict__, "batch": 1})
-        target = synth.target_logits(w1, draft_ext[:1], torch.from_numpy(t1["depth"]),
-                                     torch.from_numpy(t1["n_nodes"]), 0)
-        inp = dict(kv)
-        inp["draft"] = draft_ext[:, : w.N].contiguous()
-        inp["target"] = target
-        r = oracle_leg(w, inp, steps=args.steps, warmup=args.warmup)
-        line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": UNIT,
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": 1000.0 * r["seconds"] / r["samples"], "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": wdesc,
-                "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
-                "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
-    rt = _cudart()
-
-    # Independent input sets, rotated so that the step's inputs exceed L2.
-    # Each rank is an independent replica with its own sequences (seeds).
-    seed0 = 1000 * rank
     first, meta0 = make_set(w, seed0, dev)
     nbytes = set_bytes(first)
     R = max(1, min(16, math.ceil(2.0 * L2_BYTES / nbytes)))
@@ -428,122 +489,108 @@ def main():
         i, m = make_set(w, seed0 + s, dev)
         sets.append(i)
         metas.append(m)
-    nodes = [sum(m["n_nodes"]) for m in metas]
-
-    stream = torch.cuda.Stream(dev)
-    ex = jtree.Exec(dev)
     bufs = [StepBuffers(w, dev) for _ in range(R)]   # each set keeps its own tree / mask
-    K, Wm = args.steps, args.warmup
     with torch.cuda.stream(stream):
         for i in range(max(Wm, R)):
             run_step(w, sets[i % R], bufs[i % R], ex)
     stream.synchronize()
     if ex.read_error() != 0:
-        raise RuntimeError("device error flag set during warm-up")
+        raise RuntimeError(f"device error flag set during warm-up ({w.name})")
     acc_rows = [int(b_.acc["acc_len"].sum().item()) + w.batch for b_ in bufs]  # rows on the paths
 
-    sptr = ctypes.c_void_p(stream.cuda_stream)
+    def steps():
+        for i in range(K):
+            fns = call_fns(w, jtree_mod(), sets[i % R], bufs[i % R], ex)
+            for c in CALLS:
+                fns[c]()
 
-    def call_fns(inp, bf):
-        return {
-            "jt_topw": lambda: jtree.jt_topw(inp["draft"], w.W, bf.tok, bf.logp, exec=ex),
-            "jt_tree_expand": lambda: jtree.jt_tree_expand(bf.tok, bf.logp, w.B, out=bf.tree,
-                                                           exec=ex),
-            "jt_tree_mask": lambda: jtree.jt_tree_mask(bf.tree["parent"], bf.tree["n_nodes"],
-                                                       bf.mask, exec=ex),
-            "jt_tree_attn": lambda: jtree.jt_tree_attn(
-                inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"], inp["v_cache"],
-                inp["prefix_len"], bf.tree["n_nodes"], bf.mask, out=bf.attn_out,
-                block_table=inp["block_table"], exec=ex),
-            "jt_tree_accept": lambda: jtree.jt_tree_accept(inp["target"], bf.tree["parent"],
-                                                           bf.tree["token"], bf.tree["n_nodes"],
-                                                           w.N, out=bf.acc, exec=ex),
-        }
-
-    def capture(only=None):
-        """K steps (only=None) or K launches of one call, events at the two ends."""
-        events = [ctypes.c_void_p(), ctypes.c_void_p()]
-        for ev in events:
-            _ok(rt.cudaEventCreateWithFlags(ctypes.byref(ev), 0), "cudaEventCreateWithFlags")
-        g = Graph(rt, stream)
-        with torch.cuda.stream(stream):
-            with g:
-                _ok(rt.cudaEventRecordWithFlags(events[0], sptr, 1), "cudaEventRecordWithFlags")
-                for i in range(K):
-                    fns = call_fns(sets[i % R], bufs[i % R])
-                    for c in CALLS:
-                        if only is None or c == only:
-                            fns[c]()
-                _ok(rt.cudaEventRecordWithFlags(events[1], sptr, 1), "cudaEventRecordWithFlags")
-        g.upload()
-        return g, events
-
-    def capture_fn(fn_of_step):
-        """K launches of fn_of_step(i)(), events at the two ends."""
-        events = [ctypes.c_void_p(), ctypes.c_void_p()]
-        for ev in events:
-            _ok(rt.cudaEventCreateWithFlags(ctypes.byref(ev), 0), "cudaEventCreateWithFlags")
-        g = Graph(rt, stream)
-        with torch.cuda.stream(stream):
-            with g:
-                _ok(rt.cudaEventRecordWithFlags(events[0], sptr, 1), "cudaEventRecordWithFlags")
-                for i in range(K):
-                    fn_of_step(i)()
-                _ok(rt.cudaEventRecordWithFlags(events[1], sptr, 1), "cudaEventRecordWithFlags")
-        g.upload()
-        return g, events
-
-    def elapsed(events):
-        ms = ctypes.c_float(0)
-        _ok(rt.cudaEventElapsedTime(ctypes.byref(ms), events[0], events[1]), "cudaEventElapsedTime")
-        return ms.value
-
-    def release(g_, evs):
-        g_.close()
-        for ev in evs:
-            rt.cudaEventDestroy(ev)
-
-    g_plain, ev_plain = capture()
-    gpu_launches = g_plain.kernel_nodes()
-    stream.synchronize()
-
-    # ---- timed region (headline): K whole steps ------------------------------
     bus = ctypes.create_string_buffer(64)
-    rt.cudaDeviceGetPCIBusId(bus, 64, local)
+    timer.rt.cudaDeviceGetPCIBusId(bus, 64, local)
     sampler = ClockSampler(bus.value.decode())
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with sampler:
-        g_plain.launch()
-        stream.synchronize()
-    torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    # --------------------------------------------------------------------------
-    total_ms = elapsed(ev_plain)
-    release(g_plain, ev_plain)
-    # ---- timed regions (per call): K launches of each call alone --------------
+    total_ms, launches = timer.run(steps, dev, sampler=sampler, dist=dist)
     per_call = {}
     for c in CALLS:
-        g_c, ev_c = capture(only=c)
-        torch.cuda.synchronize(dev)
-        g_c.launch()
-        stream.synchronize()
-        per_call[c] = elapsed(ev_c) / K   # ms per launch of the call
-        release(g_c, ev_c)
+        def one(c=c):
+            for i in range(K):
+                call_fns(w, jtree_mod(), sets[i % R], bufs[i % R], ex)[c]()
+        per_call[c] = timer.run(one, dev)[0] / K     # ms per launch of the call
     if ex.read_error() != 0:
-        raise RuntimeError("device error flag set during the timed regions")
+        raise RuntimeError(f"device error flag set during the timed regions ({w.name})")
+    return {"w": w, "total_ms": total_ms, "per_call": per_call, "launches": launches,
+            "nodes": [sum(m["n_nodes"]) for m in metas], "metas": metas, "acc_rows": acc_rows,
+            "R": R, "nbytes": nbytes, "sets": sets, "bufs": bufs, "clocks": sampler.summary()}
 
-    # ---- the accepted-path K/V commit (a row beyond the step: measured alone) ----
-    # Its destinations get room for N more tokens per sequence (the workloads'
-    # caches are sized to their prefixes): a contiguous buffer, or for paged
-    # caches a small pool holding just the pages the commit writes, reached
-    # through a block table whose other entries point at page 0. The bytes
-    # moved are those of a commit into the real cache.
+
+def jtree_mod():
+    from tree_causal_verification_gb300 import jtree
+    return jtree
+
+
+def summarise(m, peaks, K):
+    """Per-call times and roofline fractions of one workload's measurement."""
+    w = m["w"]
+    works = [algorithmic_work(w, mt["prefix_len"], mt["n_nodes"], mt["depth_sum"], pr)
+             for mt, pr in zip(m["metas"], m["acc_rows"])]
+    avg = {c: {"bytes": statistics.mean(wk[c]["bytes"] for wk in works),
+               "flops": None if works[0][c]["flops"] is None
+               else statistics.mean(wk[c]["flops"] for wk in works)} for c in CALLS}
+    pc = m["per_call"]
+    calls = {}
+    for c in CALLS:
+        d = {"us": pc[c] * 1e3, "share": pc[c] / sum(pc.values()), "alg_bytes": avg[c]["bytes"],
+             "hbm_frac": avg[c]["bytes"] / (pc[c] / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        if avg[c]["flops"]:
+            d["alg_flops"] = avg[c]["flops"]
+            d["tensor_frac"] = avg[c]["flops"] / (pc[c] / 1e3) / (peaks["bf16_tflops"] * 1e12)
+        calls[c] = d
+    dom = max(CALLS, key=lambda c: pc[c])
+    # Per-call durations come from each call timed alone: burst peaks apply.
+    tensor = avg[dom]["flops"] is not None and avg[dom]["flops"] / (peaks["bf16_tflops"] * 1e12) \
+        > avg[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if tensor:
+        roof = {"kernel": dom, "bound": "tensor",
+                "achieved": avg[dom]["flops"] / (pc[dom] / 1e3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": avg[dom]["bytes"] / (pc[dom] / 1e3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = committed_traffic(dom, w.name)
+    roof["peak_source"] = peaks["source"] + (" burst" if tensor else " copy")
+    roof["algorithmic_per_launch"] = avg[dom]["flops"] if tensor else avg[dom]["bytes"]
+    nodes_per_step = statistics.mean(m["nodes"])
+    my_nodes = sum(m["nodes"][i % m["R"]] for i in range(K))
+    return {"roofline": roof, "calls": calls, "nodes_per_step": nodes_per_step,
+            "my_nodes": my_nodes, "ms_per_step": m["total_ms"] / K}
+
+
+def l2_note(m):
+    R, nbytes = m["R"], m["nbytes"]
+    return (f"{R} rotating input sets of {nbytes / 1e6:.1f} MB ({R * nbytes / 1e6:.0f} MB > "
+            f"129 MB L2)" if R > 1 else f"inputs of {nbytes / 1e6:.0f} MB per step exceed the "
+            f"129 MB L2")
+
+
+def workload_desc(w):
+    return {"workload": w.name, "batch": w.batch, "prefix": [w.prefix_lo, w.prefix_hi],
+            "B": w.B, "N": w.N, "W": w.W, "hq": w.hq, "hkv": w.hkv, "head_dim": w.D,
+            "vocab": w.V, "paged": w.paged}
+
+
+def next_rows_of(w, m, K, dev, timer, ex, peaks):
+    """Rows beyond the step, each call timed alone (K launches in a graph)."""
+    import torch
+    jtree = jtree_mod()
+    sets, bufs, R = m["sets"], m["bufs"], m["R"]
+    # The accepted-path K/V commit. Its destinations get room for N more
+    # tokens per sequence (the workloads' caches are sized to their
+    # prefixes): a contiguous buffer, or for paged caches a small pool holding
+    # just the pages the commit writes, reached through a block table whose
+    # other entries point at page 0. The bytes moved are those of a commit
+    # into the real cache.
     commit_sets = []
     for i in range(R):
-        inp, bf = sets[i], bufs[i]
+        inp = sets[i]
         L = inp["prefix_len"].cpu()
         if w.paged:
             span = (w.N + 15) // 16 + 1
@@ -609,79 +656,31 @@ def main():
         return lambda: jtree.jt_lmhead_topw(hid[i % R], w_lm, w.W, tok=lm_tok[i % R],
                                             logp=lm_logp[i % R], exec=ex)
 
-    next_ms = {}
-    with torch.cuda.stream(stream):
+    fns = (("jt_tree_commit_kv", commit_fn), ("jt_topw_entropy", entropy_fn),
+           ("jt_tree_expand_scored", scored_fn), ("jt_tree_accept_sampled", sampled_fn),
+           ("jt_lmhead_topw", lmhead_fn))
+    with torch.cuda.stream(timer.stream):
         for i in range(R):
-            for fn in (commit_fn, entropy_fn, scored_fn, sampled_fn, lmhead_fn):
+            for _, fn in fns:
                 fn(i)()
-    stream.synchronize()
+    timer.stream.synchronize()
     if ex.read_error() != 0:
         raise RuntimeError("device error flag set by a next-row call")
-    for name, fn in (("jt_tree_commit_kv", commit_fn), ("jt_topw_entropy", entropy_fn),
-                     ("jt_tree_expand_scored", scored_fn), ("jt_tree_accept_sampled", sampled_fn),
-                     ("jt_lmhead_topw", lmhead_fn)):
-        g_c, ev_c = capture_fn(fn)
-        torch.cuda.synchronize(dev)
-        g_c.launch()
-        stream.synchronize()
-        next_ms[name] = elapsed(ev_c) / K
-        release(g_c, ev_c)
+    next_ms = {}
+    for name, fn in fns:
+        def body(fn=fn):
+            for i in range(K):
+                fn(i)()
+        next_ms[name] = timer.run(body, dev)[0] / K
     commit_ms = next_ms["jt_tree_commit_kv"]
     acc_tokens_sets = [int(bf.acc["acc_len"].sum().item()) for bf in bufs]
     commit_bytes = statistics.mean(acc_tokens_sets) * 2 * 2 * 2 * w.hkv * w.D  # K,V; read+write
-
-    my_nodes = sum(nodes[i % R] for i in range(K))
-    value = job_throughput(my_nodes, total_ms / 1000.0, dev)   # all ranks' nodes / slowest rank
-    total_ms = max_over_ranks(total_ms, dev)
-
-    # Roofline of the dominant call.
-    peaks = load_peaks()
-    works = [algorithmic_work(w, m["prefix_len"], m["n_nodes"], m["depth_sum"], pr)
-             for m, pr in zip(metas, acc_rows)]
-    avg_work = {c: {"bytes": statistics.mean(wk[c]["bytes"] for wk in works),
-                    "flops": None if works[0][c]["flops"] is None
-                    else statistics.mean(wk[c]["flops"] for wk in works)} for c in CALLS}
-    dom = max(CALLS, key=lambda c: per_call[c])
-    # Per-call durations come from each call timed alone: burst peaks apply.
-    attn_tensor = avg_work["jt_tree_attn"]["flops"] / (
-        peaks["bf16_tflops"] * 1e12) > avg_work["jt_tree_attn"]["bytes"] / (
-        peaks["hbm_gbs"] * 1e9)
-    if dom == "jt_tree_attn" and attn_tensor:
-        achieved = avg_work[dom]["flops"] / (per_call[dom] / 1e3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        achieved = avg_work[dom]["bytes"] / (per_call[dom] / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = committed_traffic(dom, w.name)
-    roof["peak_source"] = peaks["source"] + (" burst" if roof["bound"] == "tensor" else "")
-    roof["algorithmic_per_launch"] = avg_work[dom]["flops"] if roof["bound"] == "tensor" \
-        else avg_work[dom]["bytes"]
-
-    calls_out = {}
-    for c in CALLS:
-        d = {"us": per_call[c] * 1e3, "share": per_call[c] / sum(per_call.values()),
-             "alg_bytes": avg_work[c]["bytes"],
-             "hbm_frac": avg_work[c]["bytes"] / (per_call[c] / 1e3) / 1e9 / peaks["hbm_gbs"]}
-        if avg_work[c]["flops"]:
-            d["alg_flops"] = avg_work[c]["flops"]
-            d["tensor_frac"] = avg_work[c]["flops"] / (per_call[c] / 1e3) / (
-                peaks["bf16_tflops"] * 1e12)
-        calls_out[c] = d
-
-    topw_b = avg_work["jt_topw"]["bytes"] + w.batch * w.N * 4
+    topw_b = w.batch * w.N * (4 * w.V + 8 * w.W) + w.batch * w.N * 4
     lm_rows = w.batch * w.N
     lm_bytes = w.V * d_model * 2 + lm_rows * d_model * 2 + lm_rows * w.W * 8
     lm_flops = 2.0 * lm_rows * d_model * w.V
     lm_s = next_ms["jt_lmhead_topw"] / 1e3
-    lm_row = {"us": lm_s * 1e6, "alg_bytes": lm_bytes, "alg_flops": lm_flops,
-              "hbm_frac": lm_bytes / lm_s / 1e9 / peaks["hbm_gbs"],
-              "tensor_frac": lm_flops / lm_s / (peaks["bf16_tflops"] * 1e12),
-              "note": ("draft hidden [batch*N][4096] x synthetic LM head [vocab][4096] bf16, "
-                       "top-W per row without writing logits; not in the step")}
-    next_rows = {
+    return {
         "jt_tree_commit_kv": {
             "us": commit_ms * 1e3, "alg_bytes": commit_bytes,
             "hbm_frac": commit_bytes / (commit_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
@@ -693,19 +692,37 @@ def main():
         "jt_tree_expand_scored": {
             "us": next_ms["jt_tree_expand_scored"] * 1e3,
             "note": "hybrid score (alpha 0.5) expansion; not in the step"},
-        "jt_lmhead_topw": lm_row,
+        "jt_lmhead_topw": {
+            "us": lm_s * 1e6, "alg_bytes": lm_bytes, "alg_flops": lm_flops,
+            "hbm_frac": lm_bytes / lm_s / 1e9 / peaks["hbm_gbs"],
+            "tensor_frac": lm_flops / lm_s / (peaks["bf16_tflops"] * 1e12),
+            "note": ("draft hidden [batch*N][4096] x synthetic LM head [vocab][4096] bf16, "
+                     "top-W per row without writing logits; not in the step")},
         "jt_tree_accept_sampled": {
             "us": next_ms["jt_tree_accept_sampled"] * 1e3,
             "note": ("temperature-1 acceptance (one Gumbel-max draw per visited node, "
                      "counter-based noise for every logit it scans); not in the step")},
     }
 
-    # ---- end to end through the public API with host buffers ---------------
-    e2e_steps = args.e2e_steps or max(3, min(K, 200))
-    host = {k: (None if t is None else t.cpu().pin_memory()) for k, t in sets[0].items()}
-    devb = {k: (None if t is None else torch.empty_like(t)) for k, t in sets[0].items()}
+
+def end_to_end(w, m, K, dev, stream, ex, e2e_steps, dist=None):
+    """The same metric through the public API with host buffers: every step
+    copies its inputs from pinned host memory, runs the five calls and reads
+    the accepted tokens back (synchronising, as a caller would)."""
+    import torch
+    from tree_causal_verification_gb300.step import run_step
+    src = m["sets"][0]
+    host = {}
+    for k, t in src.items():
+        if t is None:
+            host[k] = None
+        else:
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            host[k] = h
+    devb = {k: (None if t is None else torch.empty_like(t)) for k, t in src.items()}
     res_keys = ["acc_len", "acc_tokens", "bonus"]
-    buf = bufs[0]
+    buf = m["bufs"][0]
     res_host = {k: torch.empty(buf.acc[k].shape, dtype=buf.acc[k].dtype).pin_memory()
                 for k in res_keys}
     n_host = torch.empty((w.batch,), dtype=torch.int32).pin_memory()
@@ -729,30 +746,166 @@ def main():
         for _ in range(e2e_steps):
             e2e_step()
         e2e_s = time.perf_counter() - t0
-    e2e_value = job_throughput(e2e_steps * nodes[0], e2e_s, dev)
-    e2e = {"value": e2e_value, "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    del devb, host
+    from tree_causal_verification_gb300.dist import job_throughput
+    return {"value": job_throughput(e2e_steps * m["nodes"][0], e2e_s, dev), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
+
+# --------------------------------------------------------------------------
+# The reference arm: the CPU oracle alone.
+# --------------------------------------------------------------------------
+def reference_arm(args, w, rank):
+    if rank != 0:
+        return
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"   # input generation only
+    inp, meta = make_oracle_set(w, 0, dev)
+    threads = host_cores()
+    seqs = [i % w.batch for i in range(args.steps)]
+    r = oracle_timing(w, inp, seqs, threads, warmup=args.warmup)
+    value = r["nodes"] / r["seconds"]
+    sample = describe_oracle(w, r, threads, whole=False) + \
+        f"; {args.warmup} untimed warm-up sequence step(s)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * r["seconds"] / len(r["seqs"]), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(workload_desc(w), step="one sequence's whole step per timed step"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def make_oracle_set(w, seed, dev):
+    """The benchmark's inputs for the oracle alone: drawn like make_set (on the
+    GPU when there is one, so the bytes are the GPU arm's), with the target
+    rows drawn for the oracle's own tree."""
+    import torch
+
+    import oracle
+    from tree_causal_verification_gb300 import synth
+    draft_ext = synth.draft_logits(w, seed, dev)
+    kv = synth.kv_inputs(w, seed, dev)
+    oracle.build()
+    tok, logp = oracle.topw(draft_ext[:, : w.N].cpu().numpy(), w.W)
+    tree = oracle.tree_expand(tok, logp, w.B)
+    target = synth.target_logits(w, draft_ext, torch.from_numpy(tree["depth"]),
+                                 torch.from_numpy(tree["n_nodes"]), seed)
+    inp = dict(kv)
+    inp["draft"] = draft_ext[:, : w.N].contiguous()
+    inp["target"] = target
+    return inp, {"n_nodes": tree["n_nodes"].tolist()}
+
+
+# --------------------------------------------------------------------------
+# Main.
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="jtree", choices=["jtree", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only the headline workload")
+    ap.add_argument("--no-next-rows", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    import torch
+    from tree_causal_verification_gb300 import jtree, synth
+    from tree_causal_verification_gb300.dist import job_throughput, max_over_ranks, rank_world
+
+    rank, world, local = rank_world()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w, rank)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    rt = _cudart()
+    stream = torch.cuda.Stream(dev)
+    timer = Timer(rt, stream)
+    ex = jtree.Exec(dev)
+    K, Wm = args.steps, args.warmup
+    peaks = load_peaks()
+
+    # ---- headline workload (each rank an independent replica) ----
+    m = measure(w, K, Wm, dev, stream, timer, ex, seed0=1000 * rank, dist=dist, local=local)
+    sm = summarise(m, peaks, K)
+    value = job_throughput(sm["my_nodes"], m["total_ms"] / 1000.0, dev)
+    total_ms = max_over_ranks(m["total_ms"], dev)
+    next_rows = None if args.no_next_rows else next_rows_of(w, m, K, dev, timer, ex, peaks)
+    e2e = end_to_end(w, m, K, dev, stream, ex, args.e2e_steps or max(3, min(K, 50)), dist)
+    cpu_inp = m["sets"][0]
+    launches, clocks = m["launches"], m["clocks"]
+    wdesc = workload_desc(w)
+    wdesc["l2"] = l2_note(m)
+    wdesc["nodes_per_step"] = sm["nodes_per_step"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = oracle_leg(w, sets[0])
-        cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        threads = host_cores()
+        r = oracle_timing(w, cpu_inp, list(range(w.batch)), threads, budget_s=15.0)
+        cpu = {"value": r["nodes"] / r["seconds"], "unit": UNIT, "cores": threads,
+               "kind": "oracle", "sample": describe_oracle(w, r, threads, whole=w.batch == 1)}
+    del m, cpu_inp
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, same run (single-GPU runs only) ----
+    per_config = {}
+    if world == 1 and not args.no_per_config:
+        for name in synth.WORKLOAD_ORDER:
+            if name == w.name:
+                continue
+            wo = synth.WORKLOADS[name]
+            mo = measure(wo, K, Wm, dev, stream, timer, ex, local=local)
+            so = summarise(mo, peaks, K)
+            entry = {"value": so["my_nodes"] / (mo["total_ms"] / 1000.0), "unit": UNIT,
+                     "ms_per_step": so["ms_per_step"], "nodes_per_step": so["nodes_per_step"],
+                     "config": dict(workload_desc(wo), l2=l2_note(mo)),
+                     "roofline": so["roofline"], "calls": so["calls"], "clocks": mo["clocks"],
+                     "gpu_launches": mo["launches"]}
+            if rank == 0 and not args.no_cpu_baseline:
+                # The oracle on the whole step: all host cores, and one core
+                # where a whole step takes at most a few seconds.
+                threads = host_cores()
+                seqs = list(range(wo.batch))
+                r = oracle_timing(wo, mo["sets"][0], seqs, threads)
+                entry["cpu_baseline"] = {
+                    "value": r["nodes"] / r["seconds"], "unit": UNIT, "cores": threads,
+                    "kind": "oracle", "sample": describe_oracle(wo, r, threads, whole=True)}
+                if wo.batch == 1:
+                    r1 = oracle_timing(wo, mo["sets"][0], seqs, 1)
+                    entry["cpu_baseline_1core"] = {
+                        "value": r1["nodes"] / r1["seconds"], "unit": UNIT, "cores": 1,
+                        "kind": "oracle", "sample": describe_oracle(wo, r1, 1, whole=True)}
+            per_config[name] = entry
+            del mo
+            torch.cuda.empty_cache()
 
     if rank == 0:
-        wdesc["l2"] = (f"{R} rotating input sets of {nbytes / 1e6:.1f} MB "
-                       f"({R * nbytes / 1e6:.0f} MB > 129 MB L2)" if R > 1 else
-                       f"inputs of {nbytes / 1e6:.0f} MB per step exceed the 129 MB L2")
         wdesc["graph"] = ("K steps captured in one CUDA graph, launched once; per-call times from "
                           "one graph per call of K launches of that call alone (same input sets)")
-        wdesc["nodes_per_step"] = statistics.mean(nodes)
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
                 "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
                 "data": "synthetic (seeded, no dataset or weights)", "config": wdesc,
-                "impl": "libjtree", "roofline": roof, "calls": calls_out,
-                "next_rows": next_rows,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches * world,
-                "clocks": sampler.summary()}
+                "impl": "libjtree", "roofline": sm["roofline"], "calls": sm["calls"],
+                "next_rows": next_rows, "per_config": per_config,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * world,
+                "clocks": clocks}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -37,7 +37,9 @@
  *   the KV cache; it is not a tree node.
  * - All pointers must be 16-byte aligned.
  * - The library keeps no global state except a per-process cache of the
- *   device's attributes; it is safe to call from several host threads.
+ *   device's attributes, the wait budget of jt_set_wait_budget and the fixed
+ *   array of jt_tree_accept_noalloc; it is safe to call from several host
+ *   threads.
  */
 #ifndef JTREE_H_
 #define JTREE_H_
@@ -91,6 +93,18 @@ JT_API const char* jt_status_str(jt_status s);
  * was set, JT_ERR_DEVICE_DATA for any other flag, JT_ERR_INVALID_ARG when
  * exec or exec->d_err is NULL. */
 JT_API jt_status jt_read_device_error(const jt_exec* exec, int32_t* host_out);
+
+/* Test hook, not part of the method (the pages have no counterpart).
+ * Every wait of a kernel on an mbarrier (jt_tree_attn, jt_lmhead_topw) gives
+ * up after a budget of SM clock cycles, about 2 s by default; the CTA then
+ * sets JT_DEVERR_TIMEOUT in *exec->d_err, waits (again bounded, always with
+ * the default budget) for the TMA loads and tensor-core operations it has
+ * already issued, releases its tensor memory and finishes, leaving the
+ * context usable. This call sets the budget given to kernels launched
+ * afterwards by this process; cycles <= 0 restores the default. A budget of
+ * a few cycles makes every such call report a timeout, which is how the
+ * tests drive that path. Always returns JT_OK. */
+JT_API jt_status jt_set_wait_budget(long long cycles);
 
 /* ------------------------------------------------------------------------
  * jt_topw — top-W draft candidates per depth.
@@ -308,13 +322,17 @@ JT_API jt_status jt_tree_accept_sampled(const float* target_logits, const int32_
  * The paper has no counterpart: this is a library convenience.
  *
  * Same arguments, results and device checks as jt_tree_accept, but the
- * scratch it needs (per-row argmaxes, for chains and trees not much wider
- * than a root path) comes from a fixed array inside the library's device
- * image instead of exec->workspace (which is ignored). It is meant for
- * callers that must not call cudaMalloc or any allocating routine — for
- * example code that runs while a stream is being captured, runtimes whose
- * device memory is entirely owned by another allocator, or plain C hosts
- * with no device allocator at hand — so this call allocates nothing.
+ * scratch it needs (per-row argmaxes) comes from a fixed array inside the
+ * library's device image instead of exec->workspace (which is ignored;
+ * exec->stream and exec->d_err are used as by jt_tree_accept). It is meant
+ * for callers that must not call cudaMalloc or any allocating routine — for
+ * example runtimes whose device memory is entirely owned by another
+ * allocator, plain C hosts with no device allocator at hand, or code that
+ * cannot afford cudaMalloc's device synchronisation — so this call
+ * allocates nothing.
+ * Only chains and trees not much wider than a root path use the array:
+ * when (B+1) > 4 (n_depth+1) the call walks the accepted path without any
+ * scratch, and such calls neither touch nor race on the array.
  *
  * Limit: batch * (B + 1) <= 65536; larger requests return
  * JT_ERR_UNSUPPORTED without launching. The array (256 KiB) lives on every

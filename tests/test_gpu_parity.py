@@ -3,8 +3,11 @@
 Bit-exact: top-W indices, tree topology (parent/token/depth/n_nodes), masks,
 acceptance. Within tolerance: log-probs (1e-5 abs) and bf16 attention
 (max-abs 2e-2, mean-abs 2e-3 against the fp64 oracle). Attention is checked
-on every row for the small workloads and on sampled (sequence, node, head)
-rows for the large ones, always through the same C-ABI calls bench.py times.
+on every row of the batch-1 workloads (all 8192 (node, head) rows of the
+256-node tree). For the batched workloads every row of four whole sequences
+(the longest prefix, the shortest and two drawn at random: every KV head,
+tile pair and key-split chunk of those sequences) plus sampled rows of all
+the others, always through the same C-ABI calls bench.py times.
 """
 import numpy as np
 import pytest
@@ -16,7 +19,23 @@ from tree_causal_verification_gb300.step import StepBuffers, run_step
 
 pytestmark = pytest.mark.gpu
 
-FULL_ATTN = {"tiny", "qwen3-8b-chain"}
+FULL_ATTN = {"tiny", "qwen3-8b-chain", "high-budget"}
+
+
+def attn_rows(case):
+    """Rows compared for a workload (see the module docstring)."""
+    w = case.w
+    if w.name in FULL_ATTN:
+        return case.whole_sequences(range(w.batch))
+    L = to_np(case.kv["prefix_len"])
+    rng = np.random.default_rng(7)
+    seqs = {int(np.argmax(L)), int(np.argmin(L))}
+    rest = [b for b in range(w.batch) if b not in seqs]
+    seqs |= set(rng.choice(rest, 2, replace=False).tolist())
+    whole = case.whole_sequences(sorted(seqs))
+    sampled = case.sample_rows(case.tree["n_nodes"])
+    sampled = sampled[~np.isin(sampled[:, 0], sorted(seqs))]
+    return np.concatenate([whole, sampled])
 
 
 @pytest.fixture(scope="module", params=synth.WORKLOAD_ORDER)
@@ -62,11 +81,7 @@ def test_step_end_to_end(case):
         assert np.array_equal(to_np(buf.tree[k]), case.tree[k]), k
     np.testing.assert_allclose(to_np(buf.tree["score"]), case.tree["score"], rtol=0, atol=1e-4)
     assert np.array_equal(u32(buf.mask), case.mask)
-    if w.name in FULL_ATTN:
-        rows = np.array([(b, v, h) for b in range(w.batch) for v in range(w.B)
-                         for h in range(w.hq)], np.int32)
-    else:
-        rows = case.sample_rows(case.tree["n_nodes"])
+    rows = attn_rows(case)
     ref = case.oracle_attn(rows)
     check_attn(gather_rows(buf.attn_out, rows), ref, w.name)
     acc = case.oracle_accept()

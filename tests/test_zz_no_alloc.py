@@ -1,9 +1,10 @@
 """jt_tree_accept_noalloc: acceptance for callers that cannot allocate.
 
-Such callers (code running under stream capture, runtimes whose device memory
-belongs to another allocator, plain C hosts) cannot hand the library a
-workspace; this entry point uses a fixed device array inside the library
-instead. Its results must equal jt_tree_accept's (which takes a caller
+Such callers (runtimes whose device memory belongs to another allocator,
+plain C hosts with no device allocator, code that must not call cudaMalloc
+because it synchronises the device) cannot hand the library a workspace;
+this entry point uses a fixed device array inside the library instead. Its
+results must equal the oracle's and jt_tree_accept's (which takes a caller
 workspace) bit for bit, call after call, even though every call reuses the
 same array. Collected last (file name) so that a stop-at-first-failure run
 has already run every other test; it also passes alone in a fresh process.
@@ -34,8 +35,9 @@ def make_case(seed, batch, N, W, B, V):
             if kids and rng.random() < 0.9:
                 row = target[b, 0 if u < 0 else 1 + u]
                 row[tree["token"][b, rng.choice(kids)]] = row.max() + 1
+    ref = oracle.tree_accept(target, tree["parent"], tree["token"], tree["n_nodes"], N)
     d = lambda a: torch.from_numpy(a).to(DEV)
-    return d(target), d(tree["parent"]), d(tree["token"]), d(tree["n_nodes"]), N
+    return (d(target), d(tree["parent"]), d(tree["token"]), d(tree["n_nodes"]), N), ref
 
 
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
@@ -47,14 +49,15 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
     # there. A third, wide tree walks the path and needs no array at all.
     for seed, shape in ((1, (12, 16, 1, 16, 4096)), (2, (5, 8, 2, 24, 151936)),
                         (3, (16, 16, 4, 128, 2048))):
-        args = make_case(seed, *shape)
+        args, ref = make_case(seed, *shape)
         want = jtree.jt_tree_accept(*args, exec=ex)
         got = jtree.jt_tree_accept_noalloc(*args, exec=ex)
         torch.cuda.synchronize()
         assert ex.read_error() == 0
         for k in want:
+            assert np.array_equal(got[k].cpu().numpy(), ref[k]), (seed, k)
             assert torch.equal(got[k], want[k]), (seed, k)
-        assert int(want["acc_len"].max()) >= 2
+        assert int(ref["acc_len"].max()) >= 2
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():

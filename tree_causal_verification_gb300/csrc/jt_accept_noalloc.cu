@@ -1,13 +1,13 @@
 // jt_tree_accept_noalloc: greedy acceptance without a caller workspace.
 //
 // jt_tree_accept needs batch * (B + 1) int32 of scratch (the argmax of every
-// live target row) and takes it from exec->workspace. Some callers have no
-// way to provide that: code that never calls cudaMalloc (it synchronises the
-// device and cannot run while a stream is being captured), hosts whose device
-// memory is fully planned by an allocator they do not control, or plain C
-// embedders with no allocator at all. This entry point serves them: the
-// scratch is a fixed array in the library's own device memory image, so the
-// call allocates nothing.
+// live target row, for chains and trees not much wider than a root path) and
+// takes it from exec->workspace. Some callers have no way to provide that:
+// code that must not call cudaMalloc (it synchronises the device), hosts
+// whose device memory is fully planned by an allocator they do not control,
+// or plain C embedders with no allocator at all. This entry point serves
+// them: the scratch is a fixed array in the library's own device memory
+// image, so the call allocates nothing.
 //
 // The array is a file-scope __device__ symbol. In host code its name is only
 // a host-side stand-in, so the device address is looked up once per device
@@ -37,7 +37,12 @@ jt_status scratch_on_current_device(int* device, void** out) {
   if (!g_scratch_ptr[*device]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
-    if (e != cudaSuccess || p == nullptr) return JT_ERR_CUDA;
+    if (e != cudaSuccess || p == nullptr) {
+      // Clear the (non-sticky) error so that the caller's next, unrelated
+      // CUDA error check does not report it.
+      cudaGetLastError();
+      return JT_ERR_CUDA;
+    }
     g_scratch_ptr[*device] = p;
   }
   *out = g_scratch_ptr[*device];

@@ -1,10 +1,17 @@
 // libjtree C ABI: host-side argument validation and dispatch to the kernels.
 // Declarations and the contract of every call: include/jtree.h.
+#include <atomic>
 #include <mutex>
 
 #include "jt_internal.cuh"
 
 namespace jt {
+
+namespace {
+std::atomic<long long> g_wait_budget{kDefaultWaitBudget};
+}  // namespace
+
+long long wait_budget() { return g_wait_budget.load(std::memory_order_relaxed); }
 
 int device_sm_count(int device) {
   static std::mutex mu;
@@ -75,6 +82,11 @@ jt_status jt_read_device_error(const jt_exec* exec, int32_t* host_out) {
   *host_out = v;
   if (v == 0) return JT_OK;
   return (v & JT_DEVERR_TIMEOUT) ? JT_ERR_TIMEOUT : JT_ERR_DEVICE_DATA;
+}
+
+jt_status jt_set_wait_budget(long long cycles) {
+  g_wait_budget.store(cycles > 0 ? cycles : kDefaultWaitBudget, std::memory_order_relaxed);
+  return JT_OK;
 }
 
 size_t jt_topw_workspace_bytes(int batch, int n_depth, int vocab, int W) {

@@ -52,7 +52,8 @@
 // packed fp32x2 instruction and the row max uses the three-input max: the
 // softmax warps are bound by instruction issue, not by the exponential unit.
 // Every mbarrier wait is bounded; on expiry the CTA raises JT_DEVERR_TIMEOUT,
-// drains its outstanding MMAs, frees TMEM and finishes.
+// waits (bounded again) for the TMA loads it issued and for its outstanding
+// MMAs, frees TMEM and finishes.
 #include <cooperative_groups.h>
 #include <cuda.h>
 
@@ -75,7 +76,6 @@ constexpr int kWarpTMA = 8, kWarpMMA = 9, kWarpTMAV = 10;
 constexpr int kTile = 128;                 // query rows per M tile = keys per K/V tile
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr long long kWaitBudget = 4000000000LL;   // ~2 s at 2 GHz
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnParams {
@@ -97,6 +97,7 @@ struct AttnParams {
   __nv_bfloat16* out;
   float* part;        // split-KV partials, kPartFloats per CTA (S > 1 only)
   float scale_log2;
+  long long wait_budget;   // cycles per bounded wait (kDefaultWaitBudget unless a test shortens it)
   int32_t* d_err;
 };
 
@@ -512,7 +513,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   // Every lane of the calling warp polls; the verdict is made warp-uniform so
   // that warp-collective tcgen05 / vote instructions never see divergence.
   auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
-    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort, kWaitBudget)) != 0;
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort, p.wait_budget)) != 0;
   };
   // Valid keys of tile t (prefix tiles first, then tree tiles).
   auto tile_valid = [&](int t) {
@@ -539,6 +540,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int j_first = ks ? G : 0, j_step = ks ? 2 : 1;
   const int T_own = ks ? (T - G + 1) / 2 : T;   // key tiles this warpgroup processes
   bool sm_ok = true;
+  int issued = 0;   // producers: K (warp 8) or V (warp 10) tiles whose loads were issued
 
   if (warp >= 8) {
   // Third warpgroup: producer, MMA issuer, two idle warps. Lean registers.
@@ -562,11 +564,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       for (int jt = 0; jt < T; ++jt) {
         const int t = t_begin + jt, st = jt % kStages;
         if (jt >= kStages &&
-            !mbar_wait(&empty[st], ((jt / kStages) + 1) & 1, abort, kWaitBudget)) {
+            !mbar_wait(&empty[st], ((jt / kStages) + 1) & 1, abort, p.wait_budget)) {
           fail();
           break;
         }
         mbar_arrive_expect_tx(&full[st], QB);
+        issued = jt + 1;
         uint8_t* dst = is_v ? sV(st) : sK(st);
         if (t < p_tiles) {
           const int key0 = t * kTile;
@@ -846,6 +849,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   // take registers a softmax warpgroup still needs to grow, and deadlock.
   __syncthreads();
   if (warp >= 8) regs_inc<kRegsLaunch>();
+  // A CTA that gave up (every failing wait precedes the barrier above) may
+  // still have TMA loads landing in its shared memory. Before that memory is
+  // reused below or released at exit, each producer waits for its last load
+  // into each ring slot (a slot's earlier loads were consumed, or it would
+  // not have been refilled) and for Q, with the default budget.
+  if (*abort && lane == 0 && (warp == kWarpTMA || warp == kWarpTMAV) && T > 0) {
+    uint64_t* full = warp == kWarpTMAV ? bars->v_full : bars->k_full;
+    bool drained = warp == kWarpTMAV || mbar_wait_drain(&bars->q_full, 0, kDefaultWaitBudget);
+    for (int st = 0; st < kStages; ++st) {
+      if (issued > st) {
+        const int last = st + kStages * ((issued - 1 - st) / kStages);
+        drained &= mbar_wait_drain(&full[st], (last / kStages) & 1, kDefaultWaitBudget);
+      }
+    }
+    (void)drained;   // a load that never lands has already been reported as a timeout
+  }
   const bool have_o = warp < 8 && tile_live && sm_ok && T_own > 0;
   if (!have_o) { m_run = -INFINITY; l_run = 0.0f; }
   // Every live tile has seen its last P V complete, so the tensor pipe and
@@ -979,7 +998,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     if (*abort && lane == 0) {
       mma_commit(&bars->drain);
       const long long t0 = clock64();
-      while (!mbar_try_wait(&bars->drain, 0) && clock64() - t0 < kWaitBudget) {
+      while (!mbar_try_wait(&bars->drain, 0) && clock64() - t0 < kDefaultWaitBudget) {
       }
     }
     __syncwarp();
@@ -1026,6 +1045,7 @@ AttnParams make_params(const jt_attn_args& a) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   const float scale = a.scale != 0.0f ? a.scale : 1.0f / sqrtf((float)a.head_dim);
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_budget = wait_budget();
   return p;
 }
 

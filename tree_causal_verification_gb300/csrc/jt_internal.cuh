@@ -17,6 +17,13 @@ constexpr int kMaxW = 32;
 constexpr int kPageSize = 16;
 constexpr int kNumSMs = 152;      // GB300; the launchers query the real count
 
+// Cycle budget of the bounded device-side waits on mbarriers (about 2 s at
+// 2 GHz). jt_set_wait_budget may shorten it for kernels launched afterwards;
+// the waits that drain a CTA's own copies and MMAs after it gave up always
+// use this default.
+constexpr long long kDefaultWaitBudget = 4000000000LL;
+long long wait_budget();   // the budget kernels launched now are given
+
 // ---------------------------------------------------------------------------
 // Device error word.
 // ---------------------------------------------------------------------------

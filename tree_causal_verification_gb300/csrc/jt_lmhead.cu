@@ -38,7 +38,6 @@ constexpr int kLmABytes = kLmRows * kLmK * 2;
 constexpr int kLmBBytes = kLmN * kLmK * 2;
 constexpr int kLmStageBytes = kLmABytes + 2 * kLmBBytes;
 constexpr uint32_t kLmTmemCols = 512;
-constexpr long long kLmWaitBudget = 4000000000LL;   // ~2 s at 2 GHz
 constexpr int kMergeWarps = 8;
 
 struct LmBars {
@@ -52,7 +51,7 @@ size_t lm_smem_bytes() { return (size_t)kLmStages * kLmStageBytes + sizeof(LmBar
 template <int K, bool ENT>
 __global__ void __launch_bounds__(kLmThreads, 1)
 lmhead_tile_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
-                   int R, int d, int V, int m_tiles, int n_slices,
+                   int R, int d, int V, int m_tiles, int n_slices, long long budget,
                    ScanPartial<K>* __restrict__ part, int32_t* d_err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -87,6 +86,7 @@ lmhead_tile_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant
     if (atomicExch(&bars->abort, 1) == 0) raise_flag(d_err, JT_DEVERR_TIMEOUT);
   };
 
+  int issued = 0;   // producer: stages of A/B loads issued
   if (warp == 4) {
     // ---- TMA producer ----
     if (lane == 0) {
@@ -95,11 +95,12 @@ lmhead_tile_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant
       for (int c = 0; c < nk; ++c) {
         const int st = c % kLmStages;
         if (c >= kLmStages &&
-            !mbar_wait(&bars->empty[st], ((c / kLmStages) + 1) & 1, abort, kLmWaitBudget)) {
+            !mbar_wait(&bars->empty[st], ((c / kLmStages) + 1) & 1, abort, budget)) {
           fail();
           break;
         }
         mbar_arrive_expect_tx(&bars->full[st], kLmStageBytes);
+        issued = c + 1;
         tma_load_4d(sA(st), &ma, &bars->full[st], c * kLmK, r0, 0, 0);
         tma_load_4d(sB(st, 0), &mb, &bars->full[st], c * kLmK, v0, 0, 0);
         tma_load_4d(sB(st, 1), &mb, &bars->full[st], c * kLmK, v0 + kLmN, 0, 0);
@@ -111,7 +112,7 @@ lmhead_tile_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant
       constexpr uint32_t idesc = idesc_bf16(kLmRows, kLmN, 0, 0);
       for (int c = 0; c < nk; ++c) {
         const int st = c % kLmStages;
-        if (!mbar_wait(&bars->full[st], (c / kLmStages) & 1, abort, kLmWaitBudget)) {
+        if (!mbar_wait(&bars->full[st], (c / kLmStages) & 1, abort, budget)) {
           fail();
           break;
         }
@@ -135,8 +136,11 @@ lmhead_tile_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant
     top.init();
     Lse lse;
     lse.init();
-    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bars->done, 0, abort, kLmWaitBudget)) != 0;
-    if (!ok) fail();
+    // After a failure elsewhere in the CTA the accumulators are incomplete:
+    // the partial then holds no candidates (defined, and flagged).
+    const bool done = __all_sync(0xFFFFFFFFu, mbar_wait(&bars->done, 0, abort, budget)) != 0;
+    if (!done) fail();
+    const bool ok = __all_sync(0xFFFFFFFFu, done && !*abort) != 0;
     tc_fence_after();
     const int row = r0 + tid;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -185,13 +189,21 @@ lmhead_tile_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
-    tc_fence_after();
-    if (*abort && lane == 0) {   // retire every issued MMA before TMEM is released
-      const long long t0 = clock64();
-      while (!mbar_try_wait(&bars->done, 0) && clock64() - t0 < kLmWaitBudget) {
+  // After a failed wait (all of them precede the barrier above) TMA loads
+  // may still be landing in shared memory: the producer waits for the last
+  // load of each stage (earlier ones were consumed) before the CTA exits.
+  if (*abort && warp == 4 && lane == 0) {
+    for (int st = 0; st < kLmStages; ++st) {
+      if (issued > st) {
+        const int last = st + kLmStages * ((issued - 1 - st) / kLmStages);
+        mbar_wait_drain(&bars->full[st], (last / kLmStages) & 1, kDefaultWaitBudget);
       }
     }
+  }
+  if (warp == 5) {
+    tc_fence_after();
+    if (*abort && lane == 0)   // retire every issued MMA before TMEM is released
+      mbar_wait_drain(&bars->done, 0, kDefaultWaitBudget);
     __syncwarp();
     tmem_dealloc(tmem, kLmTmemCols);
   }
@@ -258,7 +270,7 @@ cudaError_t launch_k(const Ctx& c, const void* hidden, const void* w_lm, int R, 
                                        (int)lm_smem_bytes());
   if (e != cudaSuccess) return e;
   e = launch_kernel(tile, dim3(m_tiles * n_slices), dim3(kLmThreads), lm_smem_bytes(), c.stream, 1,
-                    ma, mb, R, d, V, m_tiles, n_slices, part, c.d_err);
+                    ma, mb, R, d, V, m_tiles, n_slices, wait_budget(), part, c.d_err);
   if (e != cudaSuccess) return e;
   return launch_kernel(lmhead_merge_kernel<K, ENT>, dim3((R + kMergeWarps - 1) / kMergeWarps),
                        dim3(kMergeWarps * 32), 0, c.stream, 1, (const ScanPartial<K>*)part, R,

@@ -55,17 +55,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity. Gives up after `budget` clock
-// cycles or as soon as *abort becomes non-zero; returns false then.
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity. Gives up once `budget` clock
+// cycles have passed or as soon as *abort becomes non-zero; returns false
+// then. The first look does not block and the budget is checked before every
+// (potentially suspending) try_wait, so a budget of a cycle or two fails on
+// the first phase that is not already complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort, long long budget) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (true) {
+  while (clock64() - t0 < budget) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
+  }
+  return false;
+}
+
+// Waits for the phase with the given parity for at most `budget` cycles,
+// whatever the abort flag says (used to drain copies still in flight once a
+// CTA has given up). Returns false if the budget ran out.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > budget) return false;
   }
+  return true;
 }
 
 // ---------------------------------------------------------------------------

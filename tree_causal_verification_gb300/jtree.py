@@ -35,7 +35,8 @@ EXPORTED = ["jt_status_str", "jt_read_device_error", "jt_topw_workspace_bytes", 
             "jt_tree_expand", "jt_tree_mask", "jt_tree_attn_workspace_bytes", "jt_tree_attn",
             "jt_tree_accept_workspace_bytes", "jt_tree_accept", "jt_tree_accept_noalloc",
             "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored",
-            "jt_tree_accept_sampled", "jt_lmhead_topw_workspace_bytes", "jt_lmhead_topw"]
+            "jt_tree_accept_sampled", "jt_lmhead_topw_workspace_bytes", "jt_lmhead_topw",
+            "jt_set_wait_budget"]
 JT_SCORE_LOGP, JT_SCORE_HYBRID, JT_SCORE_ENTROPY = 0, 1, 2
 
 
@@ -119,10 +120,11 @@ def load(path: str = LIB_PATH):
             lib.jt_lmhead_topw_workspace_bytes.argtypes = [_c_int] * 4
             lib.jt_lmhead_topw.argtypes = [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                            _pexec]
+            lib.jt_set_wait_budget.argtypes = [ctypes.c_longlong]
             for name in ("jt_read_device_error", "jt_topw", "jt_tree_expand", "jt_tree_mask",
                          "jt_tree_attn", "jt_tree_accept", "jt_tree_accept_noalloc",
                          "jt_tree_commit_kv", "jt_topw_entropy", "jt_tree_expand_scored",
-                         "jt_tree_accept_sampled", "jt_lmhead_topw"):
+                         "jt_tree_accept_sampled", "jt_lmhead_topw", "jt_set_wait_budget"):
                 getattr(lib, name).restype = _c_int
             _lib = lib
     return _lib
@@ -186,6 +188,12 @@ class Exec:
         if st not in (0, 4, 5):
             _check(st, "jt_read_device_error")
         return out.value
+
+
+def jt_set_wait_budget(cycles: int = 0):
+    """Test hook: cycle budget of the kernels' bounded waits for later
+    launches (0 restores the default of about 2 s)."""
+    _check(load().jt_set_wait_budget(int(cycles)), "jt_set_wait_budget")
 
 
 _default_execs = {}

@@ -18,7 +18,6 @@ No dataset, tokenizer or trained weight is used.
 from __future__ import annotations
 
 import dataclasses
-import math
 import zlib
 
 import torch
@@ -179,22 +178,5 @@ def target_logits(w: Workload, draft_ext: torch.Tensor, depth: torch.Tensor,
     return x
 
 
-def flat_sizes(w: Workload) -> dict:
-    """Element counts of every step input, used for H2D byte accounting."""
-    L = w.max_prefix
-    return {
-        "draft": w.batch * w.N * w.V,
-        "q": w.batch * w.B * w.hq * w.D,
-        "kv_tree": 2 * w.batch * w.B * w.hkv * w.D,
-        "kv_cache_max": 2 * w.batch * L * w.hkv * w.D,
-        "target": w.batch * (w.B + 1) * w.V,
-    }
-
-
-def ceil_div(a: int, b: int) -> int:
-    return -(-a // b)
-
-
 __all__ = ["Workload", "WORKLOADS", "WORKLOAD_ORDER", "PAGE_SIZE", "randn", "randn_bf16",
-           "prefix_lengths", "draft_logits", "kv_inputs", "target_logits", "flat_sizes",
-           "ceil_div", "math"]
+           "prefix_lengths", "draft_logits", "kv_inputs", "target_logits"]
