@@ -555,7 +555,9 @@ def summarise(m, peaks, K):
         roof = {"kernel": dom, "bound": "hbm", "achieved": avg[dom]["bytes"] / (pc[dom] / 1e3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = committed_traffic(dom, w.name)
+    # A recorded figure is per launch of the named workload at its own size.
+    from tree_causal_verification_gb300 import synth
+    roof["traffic"] = committed_traffic(dom, w.name) if synth.WORKLOADS.get(w.name) == w else None
     roof["peak_source"] = peaks["source"] + (" burst" if tensor else " copy")
     roof["algorithmic_per_launch"] = avg[dom]["flops"] if tensor else avg[dom]["bytes"]
     nodes_per_step = statistics.mean(m["nodes"])
@@ -815,6 +817,8 @@ def main():
                     help="measure only the headline workload")
     ap.add_argument("--no-next-rows", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the headline workload's batch (smaller profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -825,6 +829,9 @@ def main():
 
     rank, world, local = rank_world()
     w = synth.WORKLOADS[args.workload]
+    if args.batch is not None:
+        import dataclasses
+        w = dataclasses.replace(w, batch=args.batch)
     if args.impl == "reference":
         reference_arm(args, w, rank)
         return

@@ -16,17 +16,53 @@
 //    rows of the current node's children are prefetched into L2 while the
 //    current row is scanned, hiding the next level's DRAM latency.
 //  * all rows (chains and small trees, where nearly every row may be on the
-//    path): (1) argmax of every live target row with the clustered row scan
-//    of jt_topw (K = 1, no log-sum-exp) into the workspace, then (2) one warp
-//    per sequence walks, each step a warp-wide search for the matching child
-//    (__reduce_min_sync picks the lowest id).
+//    path): (1) argmax of every live target row with the row scan of jt_topw
+//    (K = 1, no log-sum-exp) into the workspace, clustered, or for few long
+//    rows as 32 segment partials per row that the walk reduces when it
+//    reaches the row, then (2) one warp per sequence walks, each step a
+//    warp-wide search for the matching child (__reduce_min_sync picks the
+//    lowest id).
 #include "jt_rowscan.cuh"
 #include "jt_sample.cuh"
 
 namespace jt {
 namespace {
 
-template <bool SAMPLED>
+// A segment's best (value, lowest index); i == INT_MAX: no element.
+struct ArgPart {
+  float v;
+  int i;
+};
+
+// Few long rows: kFlatParts CTAs per live row, no cluster; each writes its
+// segment's argmax to the scratch and the walk reduces a row's partials when
+// it reaches that row.
+template <bool SAMPLED, bool RES>
+__global__ void __launch_bounds__(kScanThreads)
+accept_argmax_flat_kernel(const float* __restrict__ target, const int32_t* __restrict__ n_nodes,
+                          int B, int V, float inv_t, uint64_t seed, ArgPart* __restrict__ parts) {
+  __shared__ ScanPartial<1> warp_parts[kScanWarps];
+  __shared__ ScanPartial<1> part;
+  const int row = blockIdx.x / kFlatParts;
+  const int seg = blockIdx.x % kFlatParts;
+  const int b = row / (B + 1), j = row % (B + 1);
+  grid_dependency_sync();
+  const int n = n_nodes[b];
+  if (n < 0 || n > B || j > n) return;   // a row the walk never reads
+  const int v4 = V >> 2;
+  const int per = (v4 + kFlatParts - 1) / kFlatParts;
+  const int lo = min(v4, seg * per), hi = min(v4, lo + per);
+  if (SAMPLED)
+    scan_to_partial<1, false, false, RES, GumbelKeys, true>(target + (size_t)row * V, lo, hi, &part,
+                                                       warp_parts,
+                                                       GumbelKeys{seed, (uint64_t)row << 32, inv_t});
+  else
+    scan_to_partial<1, false, false, RES, IdentityXf, true>(target + (size_t)row * V, lo, hi, &part,
+                                                       warp_parts);
+  if (threadIdx.x == 0) parts[blockIdx.x] = ArgPart{part.v[0], part.i[0]};
+}
+
+template <bool SAMPLED, bool RES>
 __global__ void __launch_bounds__(kScanThreads)
 accept_argmax_kernel(const float* __restrict__ target, const int32_t* __restrict__ n_nodes,
                      int B, int V, int S, float inv_t, uint64_t seed, int32_t* __restrict__ am) {
@@ -42,23 +78,35 @@ accept_argmax_kernel(const float* __restrict__ target, const int32_t* __restrict
   const int v4 = V >> 2;
   const int per = (v4 + S - 1) / S;
   const int lo = min(v4, seg * per), hi = min(v4, lo + per);
-  TopK<1> top;
-  top.init();
-  Lse lse;
-  lse.init();
   if (SAMPLED)
-    scan_segment<1, false, false, GumbelKeys>(target + (size_t)row * V, lo, hi, top, lse,
-                                              GumbelKeys{seed, (uint64_t)row << 32, inv_t});
+    scan_to_partial<1, false, false, RES, GumbelKeys>(target + (size_t)row * V, lo, hi, &part,
+                                                 warp_parts,
+                                                 GumbelKeys{seed, (uint64_t)row << 32, inv_t});
   else
-    scan_segment<1, false, false, IdentityXf, true>(target + (size_t)row * V, lo, hi, top, lse);
-  block_reduce<1, false>(top, lse, &part, warp_parts);
+    scan_to_partial<1, false, false, RES, IdentityXf, true>(target + (size_t)row * V, lo, hi, &part,
+                                                       warp_parts);
+  TopK<1> top;
+  Lse lse;
   if (cluster_reduce<1, false>(&part, S, top, lse)) am[row] = top.i[0];
 }
 
 constexpr int kWalkWarps = 4;
 
+// Argmax of row `row` from the scratch: one index per row (nparts == 1) or
+// the warp-wide best of the row's kFlatParts segment partials (value desc,
+// index asc, as everywhere else).
+__device__ __forceinline__ int row_argmax(const void* am, int nparts, size_t row, int lane) {
+  constexpr unsigned kFull = 0xFFFFFFFFu;
+  if (nparts == 1) return static_cast<const int32_t*>(am)[row];
+  ArgPart q{-INFINITY, INT_MAX};
+  if (lane < nparts) q = static_cast<const ArgPart*>(am)[row * nparts + lane];
+  const uint32_t key = q.i == INT_MAX ? 0u : order_key(q.v);
+  const uint32_t top = __reduce_max_sync(kFull, key);
+  return (int)__reduce_min_sync(kFull, (key == top && q.i != INT_MAX) ? (uint32_t)q.i : 0xFFFFFFFFu);
+}
+
 __global__ void __launch_bounds__(kWalkWarps * 32)
-accept_walk_kernel(const int32_t* __restrict__ am, const int32_t* __restrict__ parent,
+accept_walk_kernel(const void* __restrict__ am, int nparts, const int32_t* __restrict__ parent,
                    const int32_t* __restrict__ token, const int32_t* __restrict__ n_nodes,
                    int batch, int B, int N, int V, int32_t* __restrict__ acc_len,
                    int32_t* __restrict__ acc_tokens, int32_t* __restrict__ acc_nodes,
@@ -90,8 +138,8 @@ accept_walk_kernel(const int32_t* __restrict__ am, const int32_t* __restrict__ p
   __syncwarp();
   int len = 0, a = -1;
   if (!bad) {
-    const int32_t* am_b = am + (size_t)b * (B + 1);
-    a = am_b[0];
+    const size_t row0 = (size_t)b * (B + 1);
+    a = row_argmax(am, nparts, row0, lane);
     int cur = -1;
     while (len < N) {
       uint32_t cand = 0xFFFFFFFFu;
@@ -102,7 +150,7 @@ accept_walk_kernel(const int32_t* __restrict__ am, const int32_t* __restrict__ p
       if (lane == 0) { at[len] = a; an[len] = (int)c; }
       ++len;
       cur = (int)c;
-      a = am_b[1 + cur];
+      a = row_argmax(am, nparts, row0 + 1 + cur, lane);
     }
   } else if (lane == 0) {
     raise_flag(d_err, flag);
@@ -119,11 +167,6 @@ constexpr int kPathThreads = 256;
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
-
-struct ArgPart {
-  float v;
-  int i;
-};
 
 template <bool SAMPLED>
 __global__ void __launch_bounds__(kPathThreads)
@@ -252,10 +295,12 @@ bool use_path_walk(int B, int n_depth) { return (B + 1) > 4 * (n_depth + 1); }
 
 }  // namespace
 
-size_t accept_workspace_bytes(int batch, int B, int n_depth, int vocab) {
-  (void)vocab;
+size_t accept_workspace_bytes(int batch, int B, int n_depth, int vocab, int num_sms) {
   if (use_path_walk(B, n_depth)) return 0;
-  return align_up((size_t)batch * (B + 1) * sizeof(int32_t), 256);
+  const long rows = (long)batch * (B + 1);
+  if (use_flat_rows(rows, vocab, num_sms))
+    return align_up((size_t)rows * kFlatParts * sizeof(ArgPart), 256);
+  return align_up((size_t)rows * sizeof(int32_t), 256);
 }
 
 cudaError_t launch_tree_accept(const Ctx& c, const float* target, const int32_t* parent,
@@ -274,16 +319,32 @@ cudaError_t launch_tree_accept(const Ctx& c, const float* target, const int32_t*
                          token, n_nodes, B, n_depth, vocab, S, prefetch, inv_t, seed, acc_len,
                          acc_tokens, acc_nodes, bonus, c.d_err);
   }
-  int32_t* am = static_cast<int32_t*>(c.workspace);
   const long rows = (long)batch * (B + 1);
-  const int S = pick_row_split(rows, vocab / 4, c.num_sms, 16);
-  auto kern = sampled ? accept_argmax_kernel<true> : accept_argmax_kernel<false>;
-  cudaError_t e = launch_clustered(kern, (int)(rows * S), S, c.stream, target, n_nodes, B, vocab,
-                                   S, inv_t, seed, am);
+  cudaError_t e;
+  int nparts = 1;
+  if (use_flat_rows(rows, vocab, c.num_sms)) {
+    nparts = kFlatParts;
+    const bool res = use_resident(1, (vocab / 4 + kFlatParts - 1) / kFlatParts);
+    auto kern = sampled ? (res ? accept_argmax_flat_kernel<true, true>
+                               : accept_argmax_flat_kernel<true, false>)
+                        : (res ? accept_argmax_flat_kernel<false, true>
+                               : accept_argmax_flat_kernel<false, false>);
+    e = launch_kernel(kern, dim3((unsigned)(rows * kFlatParts)), dim3(kScanThreads), 0, c.stream,
+                      1, target, n_nodes, B, vocab, inv_t, seed,
+                      static_cast<ArgPart*>(c.workspace));
+  } else {
+    const int S = pick_row_split(rows, vocab / 4, c.num_sms, 16);
+    const bool res = use_resident(1, (vocab / 4 + S - 1) / S);
+    auto kern = sampled ? (res ? accept_argmax_kernel<true, true> : accept_argmax_kernel<true, false>)
+                        : (res ? accept_argmax_kernel<false, true> : accept_argmax_kernel<false, false>);
+    e = launch_clustered(kern, (int)(rows * S), S, c.stream, target, n_nodes, B, vocab, S, inv_t,
+                         seed, static_cast<int32_t*>(c.workspace));
+  }
   if (e != cudaSuccess) return e;
   return launch_kernel(accept_walk_kernel, dim3((batch + kWalkWarps - 1) / kWalkWarps),
-                       dim3(kWalkWarps * 32), 0, c.stream, 1, am, parent, token, n_nodes, batch, B,
-                       n_depth, vocab, acc_len, acc_tokens, acc_nodes, bonus, c.d_err);
+                       dim3(kWalkWarps * 32), 0, c.stream, 1, (const void*)c.workspace, nparts,
+                       parent, token, n_nodes, batch, B, n_depth, vocab, acc_len, acc_tokens,
+                       acc_nodes, bonus, c.d_err);
 }
 
 }  // namespace jt

@@ -82,6 +82,10 @@ extern "C" jt_status jt_tree_accept_noalloc(const float* target_logits, const in
   c.workspace = scratch;
   c.workspace_bytes = sizeof(int32_t) * (size_t)kNoAllocMaxRows;
   c.num_sms = device_sm_count(c.device);
+  // Whatever layout the call picks (one index per row, or per-segment
+  // partials for a few long rows) must fit the array.
+  if (accept_workspace_bytes(batch, B, n_depth, vocab, c.num_sms) > c.workspace_bytes)
+    return JT_ERR_UNSUPPORTED;
   if (batch == 0) return JT_OK;
   return launch_tree_accept(c, target_logits, parent, token, n_nodes, batch, B, n_depth, vocab,
                             acc_len, acc_tokens, acc_nodes, bonus) == cudaSuccess

@@ -263,7 +263,9 @@ jt_status jt_lmhead_topw(const void* hidden, const void* w_lm, int rows, int d, 
 
 size_t jt_tree_accept_workspace_bytes(int batch, int B, int n_depth, int vocab) {
   if (batch < 0 || B < 1 || B > kMaxB || n_depth < 1 || n_depth > kMaxDepth || vocab < 1) return 0;
-  return accept_workspace_bytes(batch, B, n_depth, vocab);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  return accept_workspace_bytes(batch, B, n_depth, vocab, device_sm_count(dev));
 }
 
 namespace {
@@ -285,7 +287,7 @@ jt_status accept_impl(const float* target_logits, const int32_t* parent, const i
   Ctx c;
   jt_status st = make_ctx(exec, &c);
   if (st != JT_OK) return st;
-  st = need_workspace(c, accept_workspace_bytes(batch, B, n_depth, vocab));
+  st = need_workspace(c, accept_workspace_bytes(batch, B, n_depth, vocab, c.num_sms));
   if (st != JT_OK) return st;
   return from_cuda(launch_tree_accept(c, target_logits, parent, token, n_nodes, batch, B, n_depth,
                                       vocab, acc_len, acc_tokens, acc_nodes, bonus, sampled,

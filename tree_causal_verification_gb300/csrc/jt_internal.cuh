@@ -90,7 +90,7 @@ cudaError_t launch_tree_expand(const Ctx&, const int32_t* tok, const float* logp
                                int32_t* depth, float* score, int32_t* n_nodes);
 cudaError_t launch_topw(const Ctx&, const float* logits, int rows, int vocab, int W, int32_t* tok,
                         float* logp, float* entropy);
-size_t accept_workspace_bytes(int batch, int B, int n_depth, int vocab);
+size_t accept_workspace_bytes(int batch, int B, int n_depth, int vocab, int num_sms);
 cudaError_t launch_tree_accept(const Ctx&, const float* target, const int32_t* parent,
                                const int32_t* token, const int32_t* n_nodes, int batch, int B,
                                int n_depth, int vocab, int32_t* acc_len, int32_t* acc_tokens,

@@ -353,15 +353,111 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
   }
 }
 
-// Reduces the CTA's per-thread state into `out` (valid after the trailing
+// Short segments: at most kResident float4s per thread, every load issued
+// at once (one round trip to memory) and the elements kept in registers.
+// The log-sum-exp runs over them as in scan_batch; the warp's top K is then
+// taken by K rounds of warp argmax over each lane's best remaining element,
+// the round's winner blanking that element (NaN, which is outside the input
+// contract and which fmaxf ignores) and rescanning its per-float4 maxima.
+// No per-element insertion (whose lane divergence dominated short scans).
+constexpr int kResident = 12;
+
+template <int K, bool LSE, bool ENT, class Xf>
+__device__ __forceinline__ void scan_resident(const float* __restrict__ row, int lo4, int hi4,
+                                              float (&wv)[K], int (&wi)[K], Lse& lse,
+                                              const Xf& xf) {
+  constexpr unsigned kFull = 0xFFFFFFFFu;
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  const int tid = (int)threadIdx.x;
+  const float nan = __int_as_float(0x7fffffff);
+  float4 x[kResident];
+#pragma unroll
+  for (int u = 0; u < kResident; ++u) {
+    const int j = lo4 + tid + u * kScanThreads;
+    x[u] = j < hi4 ? ld_stream(r4 + j) : make_float4(nan, nan, nan, nan);
+  }
+#pragma unroll
+  for (int u = 0; u < kResident; ++u) {
+    const int j = lo4 + tid + u * kScanThreads;
+    if (j < hi4) x[u] = xf(x[u], j);
+  }
+  float sm[kResident];   // slot maxima; NaN for padding (and, later, emptied slots)
+#pragma unroll
+  for (int u = 0; u < kResident; ++u) sm[u] = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+  if (LSE) {
+    float bm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kResident; ++u) bm = fmaxf(bm, sm[u]);
+    const float bm2 = bm * kLog2e;
+    if (bm2 > lse.m) lse.raise<ENT>(bm2);
+    if (lse.m != -INFINITY) {
+      const float nm = -lse.m;
+      float a0 = 0.0f, a1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
+#pragma unroll
+      for (int u = 0; u < kResident; ++u) {
+        if (lo4 + tid + u * kScanThreads < hi4) {
+          a0 += lse.term<ENT>(fmaf(x[u].x, kLog2e, nm), t0) +
+                lse.term<ENT>(fmaf(x[u].y, kLog2e, nm), t1);
+          a1 += lse.term<ENT>(fmaf(x[u].z, kLog2e, nm), t0) +
+                lse.term<ENT>(fmaf(x[u].w, kLog2e, nm), t1);
+        }
+      }
+      lse.s += a0 + a1;
+      if (ENT) lse.t += t0 + t1;
+    }
+  }
+  // The lane's best remaining element: the first slot with the highest
+  // maximum (slots rise with the element index), then its first element
+  // equal to that maximum. bu < 0: nothing left.
+  int bu = -1;
+  float bmx = 0.0f;
+  auto find_best = [&]() {
+    bu = -1;
+#pragma unroll
+    for (int u = 0; u < kResident; ++u)
+      if (sm[u] == sm[u] && (bu < 0 || sm[u] > bmx)) { bmx = sm[u]; bu = u; }
+  };
+  find_best();
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    int idx = INT_MAX, c = 0;
+    if (bu >= 0) {
+      float4 q = x[0];
+#pragma unroll
+      for (int u = 1; u < kResident; ++u)
+        if (u == bu) q = x[u];
+      c = q.x == bmx ? 0 : q.y == bmx ? 1 : q.z == bmx ? 2 : 3;
+      idx = 4 * (lo4 + tid + bu * kScanThreads) + c;
+    }
+    const uint32_t key = bu >= 0 ? order_key(bmx) : 0u;
+    const uint32_t top = __reduce_max_sync(kFull, key);
+    const uint32_t win = __reduce_min_sync(kFull, (bu >= 0 && key == top) ? (uint32_t)idx : 0xFFFFFFFFu);
+    wv[k] = top == 0 ? -INFINITY : key_value(top);
+    wi[k] = top == 0 ? INT_MAX : (int)win;
+    if (k + 1 < K && bu >= 0 && (uint32_t)idx == win) {
+#pragma unroll
+      for (int u = 0; u < kResident; ++u) {
+        if (u == bu) {
+          if (c == 0) x[u].x = nan;
+          else if (c == 1) x[u].y = nan;
+          else if (c == 2) x[u].z = nan;
+          else x[u].w = nan;
+          sm[u] = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+        }
+      }
+      find_best();
+    }
+  }
+}
+
+// Reduces the warps' sorted top-K lists (identical in every lane of a warp)
+// and the threads' log-sum-exp states into `out` (valid after the trailing
 // __syncthreads).
 template <int K, bool LSE>
-__device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial<K>* out,
-                                             ScanPartial<K>* warp_parts) {
+__device__ __forceinline__ void block_reduce_lists(const float (&wv)[K], const int (&wi)[K],
+                                                   Lse& lse, ScanPartial<K>* out,
+                                                   ScanPartial<K>* warp_parts) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float wv[K];
-  int wi[K];
-  warp_select<K, K>(top.v, top.i, min(top.n, K), wv, wi);
   if (LSE) lse.warp_reduce();
   if (lane == 0) {
 #pragma unroll
@@ -406,6 +502,43 @@ __device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial
     }
   }
   __syncthreads();
+}
+
+// Reduces the CTA's per-thread state into `out` (valid after the trailing
+// __syncthreads).
+template <int K, bool LSE>
+__device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial<K>* out,
+                                             ScanPartial<K>* warp_parts) {
+  float wv[K];
+  int wi[K];
+  warp_select<K, K>(top.v, top.i, min(top.n, K), wv, wi);
+  block_reduce_lists<K, LSE>(wv, wi, lse, out, warp_parts);
+}
+
+// Whether segments of seg4 float4s take the register-resident scan (a
+// separate kernel instance, so that the streaming one keeps its registers).
+inline bool use_resident(int K, int seg4) { return K <= 8 && seg4 <= kResident * kScanThreads; }
+
+// A CTA's scan of [lo4, hi4) of a row into `part`: the register-resident
+// scan (RES, segments of at most kResident float4s per thread) or the
+// streaming scan.
+template <int K, bool LSE, bool ENT, bool RES, class Xf = IdentityXf, bool EARLY_TAIL = false>
+__device__ __forceinline__ void scan_to_partial(const float* __restrict__ row, int lo4, int hi4,
+                                                ScanPartial<K>* part, ScanPartial<K>* warp_parts,
+                                                const Xf& xf = Xf()) {
+  Lse lse;
+  lse.init();
+  if (RES) {
+    float wv[K];
+    int wi[K];
+    scan_resident<K, LSE, ENT>(row, lo4, hi4, wv, wi, lse, xf);
+    block_reduce_lists<K, LSE>(wv, wi, lse, part, warp_parts);
+  } else {
+    TopK<K> top;
+    top.init();
+    scan_segment<K, LSE, ENT, Xf, EARLY_TAIL>(row, lo4, hi4, top, lse, xf);
+    block_reduce<K, LSE>(top, lse, part, warp_parts);
+  }
 }
 
 // Merges the cluster's partials in CTA rank 0 (warp 0). Returns true in the
@@ -457,6 +590,16 @@ __device__ __forceinline__ bool cluster_reduce(ScanPartial<K>* mine, int S, TopK
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   return holder;
+}
+
+// Few long rows (fewer than two waves of 16-CTA clusters, rows of at least
+// 64K elements) are cut into kFlatParts segments with no cluster: each CTA's
+// segment is then at most one full batch plus a tail, all loaded in one
+// round trip, and its partial goes to global scratch for a later merge.
+constexpr int kFlatParts = 32;
+
+inline bool use_flat_rows(long rows, int V, int num_sms) {
+  return rows * 16 < 2L * num_sms && V / 4 >= 16 * 1024;
 }
 
 // Picks the cluster size (segments per row) for `rows` rows of `v4` float4s:

@@ -19,7 +19,7 @@
 namespace jt {
 namespace {
 
-template <int K, bool ENT>
+template <int K, bool ENT, bool RES>
 __global__ void __launch_bounds__(kScanThreads)
 topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __restrict__ tok,
             float* __restrict__ logp, float* __restrict__ entropy) {
@@ -30,13 +30,10 @@ topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __re
   const int v4 = V >> 2;
   const int per = (v4 + S - 1) / S;
   const int lo = min(v4, seg * per), hi = min(v4, lo + per);
-  TopK<K> top;
-  top.init();
-  Lse lse;
-  lse.init();
   grid_dependency_sync();
-  scan_segment<K, true, ENT>(logits + (size_t)row * V, lo, hi, top, lse);
-  block_reduce<K, true>(top, lse, &part, warp_parts);
+  scan_to_partial<K, true, ENT, RES>(logits + (size_t)row * V, lo, hi, &part, warp_parts);
+  TopK<K> top;
+  Lse lse;
   if (cluster_reduce<K, true>(&part, S, top, lse)) {
     // lse.m is the max of x*log2(e) and lse.s = sum 2^(x*log2(e) - m), so
     // ln Z = m * ln 2 + ln s.
@@ -58,11 +55,10 @@ template <int K>
 cudaError_t launch_k(const Ctx& c, const float* logits, int rows, int V, int W, int32_t* tok,
                      float* logp, float* entropy) {
   const int S = pick_row_split(rows, V / 4, c.num_sms, 16);
-  if (entropy)
-    return launch_clustered(topw_kernel<K, true>, rows * S, S, c.stream, logits, V, W, S, tok,
-                            logp, entropy);
-  return launch_clustered(topw_kernel<K, false>, rows * S, S, c.stream, logits, V, W, S, tok, logp,
-                          entropy);
+  const bool res = use_resident(K, (V / 4 + S - 1) / S);
+  auto kern = entropy ? (res ? topw_kernel<K, true, true> : topw_kernel<K, true, false>)
+                      : (res ? topw_kernel<K, false, true> : topw_kernel<K, false, false>);
+  return launch_clustered(kern, rows * S, S, c.stream, logits, V, W, S, tok, logp, entropy);
 }
 
 }  // namespace
