@@ -79,6 +79,43 @@ def test_expand_and_mask_random(batch, N, W, B):
     assert np.array_equal(u32(mask), oracle.tree_mask(ref["parent"], ref["n_nodes"]))
 
 
+def _increments(kind, rng, shape):
+    """Candidate score increments of one shape family (binary32)."""
+    if kind == "unsorted":          # ranks not in increment order
+        x = -rng.exponential(1.0, shape)
+    elif kind == "near-zero":       # many rounds; exact zeros tie with their parents
+        x = -np.sort(rng.exponential(0.05, shape), axis=-1)
+        x[..., 0] = np.where(rng.random(shape[:-1]) < 0.3, 0.0, x[..., 0])
+    elif kind == "equal":           # every node of a depth ties: level order by id
+        x = np.broadcast_to(-rng.exponential(1.0, shape[:-1])[..., None], shape).copy()
+    elif kind == "positive":        # increments above 0: children outscore parents
+        x = rng.normal(0.0, 1.0, shape)
+    elif kind == "neg-inf":         # -inf candidates (a row with fewer finite tokens than W)
+        x = -np.sort(rng.exponential(1.0, shape), axis=-1)
+        x[..., -1] = -np.inf
+        x[:, ::3, 1:] = -np.inf
+    else:                           # one dominant token per depth
+        x = -np.sort(rng.exponential(4.0, shape), axis=-1)
+        x[..., 0] = -rng.exponential(0.01, shape[:-1])
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("kind", ["unsorted", "near-zero", "equal", "positive", "neg-inf",
+                                  "dominant"])
+@pytest.mark.parametrize("batch,N,W,B", [(3, 16, 4, 256), (5, 8, 4, 64), (2, 64, 2, 255),
+                                         (4, 6, 32, 200), (7, 3, 3, 33)])
+def test_expand_increment_shapes(kind, batch, N, W, B):
+    """Expansion is the heap's best-first order whatever the increments look like."""
+    rng = np.random.default_rng(B * 31 + N * 7 + W + len(kind))
+    tok = rng.integers(0, 50000, (batch, N, W)).astype(np.int32)
+    logp = _increments(kind, rng, (batch, N, W))
+    ref = oracle.tree_expand(tok, logp, B)
+    tree = jtree.jt_tree_expand(torch.from_numpy(tok).to(DEV), torch.from_numpy(logp).to(DEV), B)
+    for k in ("parent", "token", "depth", "n_nodes"):
+        assert np.array_equal(to_np(tree[k]), ref[k]), k
+    assert np.array_equal(to_np(tree["score"]).view(np.uint32), ref["score"].view(np.uint32))
+
+
 @pytest.mark.parametrize("B", [1, 2, 31, 32, 33, 100, 255, 256])
 def test_mask_random_trees(B):
     rng = np.random.default_rng(B)

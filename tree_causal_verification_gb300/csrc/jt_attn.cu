@@ -612,9 +612,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         const uint64_t off = (uint64_t)(((kk >> 2) * CHB + (kk & 3) * 32) >> 4);
-        mma_bf16_ss(d, q + off, k + off, id_s, kk > 0);
+        mma_bf16_ss_warp(d, q + off, k + off, id_s, kk > 0);
       }
-      mma_commit(&bars->s_full[Gd]);
+      mma_commit_warp(&bars->s_full[Gd]);
     };
     // O_Gd (+)= P_Gd V, V from the slot of key tile jt; `first` starts O.
     auto issue_pv = [&](int Gd, int jt, bool first) {
@@ -622,8 +622,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       const uint32_t d = tmem + 256 + Gd * OSTRIDE, a = tmem + Gd * 128;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_bf16_ts(d, a + kk * 8, v + (uint64_t)(kk * (2048 >> 4)), id_o, !first || kk > 0);
-      mma_commit(&bars->pv_done[Gd]);
+        mma_bf16_ts_warp(d, a + kk * 8, v + (uint64_t)(kk * (2048 >> 4)), id_o, !first || kk > 0);
+      mma_commit_warp(&bars->pv_done[Gd]);
     };
     // Rows of V past a tile's valid keys that the TMA read from memory may
     // hold anything (NaN included); P is 0 there but 0 * NaN is NaN, so they
@@ -651,19 +651,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       // Key split, per key tile t (column group t & 1, local index t >> 1):
       // S(0), S(1), then PV(t), S(t + 2) for t = 0, 1, 2, ...
       tc_fence_after();
-      if (lane == 0) {
-        issue_s(0, 0, 0);
-        mma_commit(&bars->k_empty[0]);
-      }
-      __syncwarp();
+      issue_s(0, 0, 0);
+      mma_commit_warp(&bars->k_empty[0]);
       if (!warp_wait(&bars->k_full[1], 0)) { fail(); ok = false; }
       if (ok) {
         tc_fence_after();
-        if (lane == 0) {
-          issue_s(0, 1, 1);
-          mma_commit(&bars->k_empty[1]);
-        }
-        __syncwarp();
+        issue_s(0, 1, 1);
+        mma_commit_warp(&bars->k_empty[1]);
       }
       for (int t = 0; ok && t < T; ++t) {
         const int Gt = t & 1, st = t % kStages;
@@ -671,30 +665,21 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         if (!warp_wait(&bars->v_full[st], (t / kStages) & 1)) { fail(); ok = false; break; }
         zero_v_tail(t);
         tc_fence_after();
-        if (lane == 0) {
-          issue_pv(Gt, t, t < 2);
-          mma_commit(&bars->v_empty[st]);
-        }
-        __syncwarp();
+        issue_pv(Gt, t, t < 2);
+        mma_commit_warp(&bars->v_empty[st]);
         if (t + 2 < T) {
           if (!warp_wait(&bars->k_full[st], ((t + 2) / kStages) & 1)) { fail(); ok = false; break; }
           tc_fence_after();
-          if (lane == 0) {
-            issue_s(0, st, Gt);
-            mma_commit(&bars->k_empty[st]);
-          }
-          __syncwarp();
+          issue_s(0, st, Gt);
+          mma_commit_warp(&bars->k_empty[st]);
         }
       }
     } else if (ok) {
       // Tile pair, per key tile jt: PV_A(jt), S_A(jt+1), PV_B(jt), S_B(jt+1).
       tc_fence_after();
-      if (lane == 0) {
-        issue_s(0, 0, 0);
-        if (twoB) issue_s(1, 0, 1);
-        mma_commit(&bars->k_empty[0]);   // K tile 0 is no longer needed
-      }
-      __syncwarp();
+      issue_s(0, 0, 0);
+      if (twoB) issue_s(1, 0, 1);
+      mma_commit_warp(&bars->k_empty[0]);   // K tile 0 is no longer needed
     }
     for (int jt = 0; ok && !ks && jt < T; ++jt) {
       const int st = jt % kStages;
@@ -702,33 +687,25 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       if (!warp_wait(&bars->v_full[st], (jt / kStages) & 1)) { fail(); ok = false; break; }
       zero_v_tail(jt);
       tc_fence_after();
-      if (lane == 0) issue_pv(0, jt, jt == 0);
-      __syncwarp();
+      issue_pv(0, jt, jt == 0);
       const bool more = jt + 1 < T;
       const int st1 = (jt + 1) % kStages;
       if (more) {
         if (!warp_wait(&bars->k_full[st1], ((jt + 1) / kStages) & 1)) { fail(); ok = false; break; }
         tc_fence_after();
-        if (lane == 0) {
-          issue_s(0, st1, 0);
-          if (!twoB) mma_commit(&bars->k_empty[st1]);
-        }
-        __syncwarp();
+        issue_s(0, st1, 0);
+        if (!twoB) mma_commit_warp(&bars->k_empty[st1]);
       }
       if (twoB) {
         if (!warp_wait(&bars->p_full[1], jt & 1)) { fail(); ok = false; break; }
         tc_fence_after();
-        if (lane == 0) issue_pv(1, jt, jt == 0);
-        __syncwarp();
+        issue_pv(1, jt, jt == 0);
       }
-      if (lane == 0) {
-        mma_commit(&bars->v_empty[st]);
-        if (twoB && more) {
-          issue_s(1, st1, 1);
-          mma_commit(&bars->k_empty[st1]);
-        }
+      mma_commit_warp(&bars->v_empty[st]);
+      if (twoB && more) {
+        issue_s(1, st1, 1);
+        mma_commit_warp(&bars->k_empty[st1]);
       }
-      __syncwarp();
     }
   }
   } else {
@@ -995,8 +972,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   __syncthreads();
   if (warp == kWarpMMA) {
     tc_fence_after();
-    if (*abort && lane == 0) {
-      mma_commit(&bars->drain);
+    if (*abort) {
+      // The elected lane issued every MMA, so it also commits the drain.
+      mma_commit_warp(&bars->drain);
       const long long t0 = clock64();
       while (!mbar_try_wait(&bars->drain, 0) && clock64() - t0 < kDefaultWaitBudget) {
       }
