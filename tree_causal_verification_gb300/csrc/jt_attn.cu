@@ -19,8 +19,8 @@
 // One CTA per unit (or per slice of its key tiles when units are too few to
 // fill the GPU: split-KV over a cluster of S = 2..8 CTAs, whose fp32
 // partials meet in an L2-resident workspace across one cluster barrier). 384 threads = 3 warpgroups; setmaxnreg moves registers
-// from the third (producer / MMA, 88 each) to the two softmax warpgroups
-// (208 each) for the main loop; 384 x 168 = 256 x 208 + 128 x 88:
+// from the third (producer / MMA, 104 each) to the two softmax warpgroups
+// (200 each) for the main loop; 384 x 168 = 256 x 200 + 128 x 104:
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread r of a
 //              warpgroup owns TMEM lane r (= query row). It loads the row's
 //              128 scores of S from TMEM once, applies the prefix bound /
@@ -71,7 +71,7 @@ namespace cg = cooperative_groups;
 using namespace sm100;
 
 constexpr int kThreads = 384;
-constexpr uint32_t kRegsSoftmax = 208, kRegsOther = 88, kRegsLaunch = 168;
+constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104, kRegsLaunch = 168;
 constexpr int kWarpTMA = 8, kWarpMMA = 9, kWarpTMAV = 10;
 constexpr int kTile = 128;                 // query rows per M tile = keys per K/V tile
 constexpr int kStages = 2;
@@ -617,13 +617,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       mma_commit_warp(&bars->s_full[Gd]);
     };
     // O_Gd (+)= P_Gd V, V from the slot of key tile jt; `first` starts O.
-    auto issue_pv = [&](int Gd, int jt, bool first) {
+    // Only a group's last P V is committed to pv_done (one phase per
+    // launch): the epilogue is its one reader.
+    auto issue_pv = [&](int Gd, int jt, bool first, bool last) {
       const uint64_t v = vd[jt % kStages];
       const uint32_t d = tmem + 256 + Gd * OSTRIDE, a = tmem + Gd * 128;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_bf16_ts_warp(d, a + kk * 8, v + (uint64_t)(kk * (2048 >> 4)), id_o, !first || kk > 0);
-      mma_commit_warp(&bars->pv_done[Gd]);
+      if (last) mma_commit_warp(&bars->pv_done[Gd]);
     };
     // Rows of V past a tile's valid keys that the TMA read from memory may
     // hold anything (NaN included); P is 0 there but 0 * NaN is NaN, so they
@@ -665,7 +667,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         if (!warp_wait(&bars->v_full[st], (t / kStages) & 1)) { fail(); ok = false; break; }
         zero_v_tail(t);
         tc_fence_after();
-        issue_pv(Gt, t, t < 2);
+        issue_pv(Gt, t, t < 2, t + 2 >= T);
         mma_commit_warp(&bars->v_empty[st]);
         if (t + 2 < T) {
           if (!warp_wait(&bars->k_full[st], ((t + 2) / kStages) & 1)) { fail(); ok = false; break; }
@@ -683,23 +685,33 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     }
     for (int jt = 0; ok && !ks && jt < T; ++jt) {
       const int st = jt % kStages;
-      if (!warp_wait(&bars->p_full[0], jt & 1)) { fail(); ok = false; break; }
-      if (!warp_wait(&bars->v_full[st], (jt / kStages) & 1)) { fail(); ok = false; break; }
-      zero_v_tail(jt);
-      tc_fence_after();
-      issue_pv(0, jt, jt == 0);
       const bool more = jt + 1 < T;
       const int st1 = (jt + 1) % kStages;
+      // The loads run well ahead of the MMAs: observe V(jt) and K(jt+1)
+      // first, so that only the MMAs follow the wait for P_A (the tile's
+      // softmax -> P V -> S -> softmax chain sets the pace).
+      // One combined test (both normally landed long ago); the bounded
+      // waits only when it fails.
+      const bool kv = mbar_test_wait(&bars->v_full[st], (jt / kStages) & 1) &
+                      (!more || mbar_test_wait(&bars->k_full[st1], ((jt + 1) / kStages) & 1));
+      if (!__all_sync(0xFFFFFFFFu, kv)) {
+        if (!warp_wait(&bars->v_full[st], (jt / kStages) & 1)) { fail(); ok = false; break; }
+        if (more && !warp_wait(&bars->k_full[st1], ((jt + 1) / kStages) & 1)) {
+          fail(); ok = false; break;
+        }
+      }
+      zero_v_tail(jt);
+      if (!warp_wait(&bars->p_full[0], jt & 1)) { fail(); ok = false; break; }
+      tc_fence_after();
+      issue_pv(0, jt, jt == 0, !more);
       if (more) {
-        if (!warp_wait(&bars->k_full[st1], ((jt + 1) / kStages) & 1)) { fail(); ok = false; break; }
-        tc_fence_after();
         issue_s(0, st1, 0);
         if (!twoB) mma_commit_warp(&bars->k_empty[st1]);
       }
       if (twoB) {
         if (!warp_wait(&bars->p_full[1], jt & 1)) { fail(); ok = false; break; }
         tc_fence_after();
-        issue_pv(1, jt, jt == 0);
+        issue_pv(1, jt, jt == 0, !more);
       }
       mma_commit_warp(&bars->v_empty[st]);
       if (twoB && more) {
@@ -713,24 +725,26 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   regs_inc<kRegsSoftmax>();
   if (tile_live) {
     const bool row_valid = v < n;
-    uint32_t mrow[kMaxWords];
-#pragma unroll
-    for (int w = 0; w < kMaxWords; ++w)
-      mrow[w] = (row_valid && w < p.words) ? p.mask[((size_t)b * p.B + v) * p.words + w] : 0u;
+    // This row's ancestor words, read for the tree tiles only (one or two
+    // per CTA), before the wait for S so that the load overlaps it.
+    const uint32_t* mrow = p.mask + ((size_t)b * p.B + (row_valid ? v : 0)) * p.words;
     const float sl2 = p.scale_log2;
     for (int jt = j_first, it = 0; jt < T; jt += j_step, ++it) {
       const int t = t_begin + jt;
-      if (!warp_wait(&bars->s_full[G], it & 1)) { fail(); sm_ok = false; break; }
-      tc_fence_after();
       // Which keys of this tile the row sees: c < lim, and for tree tiles the
       // ancestor bit of key u0 + c.
       const bool tree = t >= p_tiles;
       const int lim = tree ? n - (t - p_tiles) * kTile : L - t * kTile;
-      const bool hi = tree && ((t - p_tiles) * kTile) >= 128;
-      const uint32_t ws0 = tree ? (hi ? mrow[4] : mrow[0]) : 0xFFFFFFFFu;
-      const uint32_t ws1 = tree ? (hi ? mrow[5] : mrow[1]) : 0xFFFFFFFFu;
-      const uint32_t ws2 = tree ? (hi ? mrow[6] : mrow[2]) : 0xFFFFFFFFu;
-      const uint32_t ws3 = tree ? (hi ? mrow[7] : mrow[3]) : 0xFFFFFFFFu;
+      const int wb = tree && ((t - p_tiles) * kTile) >= 128 ? 4 : 0;
+      uint32_t ws0 = 0xFFFFFFFFu, ws1 = 0xFFFFFFFFu, ws2 = 0xFFFFFFFFu, ws3 = 0xFFFFFFFFu;
+      if (tree) {
+        ws0 = row_valid && wb + 0 < p.words ? __ldg(mrow + wb + 0) : 0u;
+        ws1 = row_valid && wb + 1 < p.words ? __ldg(mrow + wb + 1) : 0u;
+        ws2 = row_valid && wb + 2 < p.words ? __ldg(mrow + wb + 2) : 0u;
+        ws3 = row_valid && wb + 3 < p.words ? __ldg(mrow + wb + 3) : 0u;
+      }
+      if (!warp_wait(&bars->s_full[G], it & 1)) { fail(); sm_ok = false; break; }
+      tc_fence_after();
       auto word_of = [&](int c) {   // ancestor bits of keys 32c..32c+31 of this tile
         const uint32_t w01 = (c & 1) ? ws1 : ws0, w23 = (c & 1) ? ws3 : ws2;
         return (c & 2) ? w23 : w01;
@@ -814,7 +828,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       if (lane == 0) mbar_arrive(&bars->p_full[G]);
     }
     if (sm_ok && T_own > 0) {
-      if (warp_wait(&bars->pv_done[G], (T_own - 1) & 1)) tc_fence_after();
+      if (warp_wait(&bars->pv_done[G], 0)) tc_fence_after();
       else { fail(); sm_ok = false; }
     }
   }
