@@ -7,9 +7,11 @@
 // startedourmission.github.io, "How it works", s(π(v)) equation), attach up
 // to W children, push them back, until B nodes exist or nothing is left.
 //
-// GPU design: the expansion is inherently serial, so one warp owns one
-// sequence and makes every step of a pop warp-parallel instead of using a
-// heap. The frontier (created, unpopped nodes with depth < N) lives in
+// GPU design: one warp owns one sequence. Widths >= 2 pop in rounds
+// (tree_expand_rounds_kernel below: every node the heap would pop before
+// any child created in the round pops at once); the one-pop-at-a-time form
+// described here serves width 1, where the tree is a chain. Each step of a
+// pop is warp-parallel instead of a heap. The frontier (created, unpopped nodes with depth < N) lives in
 // registers: node v occupies lane v & 31, slot v >> 5 (B <= 256 -> 8 slots).
 // A pop is two warp reductions: __reduce_max_sync over an order-preserving
 // uint32 key of the score, then __reduce_min_sync over the ids holding that
