@@ -108,27 +108,28 @@ lmhead_tile_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant
     }
   } else if (warp == 5) {
     // ---- MMA issuer: D_n += A B_n^T, n = 0, 1 (K-major operands, K = 16 per MMA) ----
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kLmRows, kLmN, 0, 0);
-      for (int c = 0; c < nk; ++c) {
-        const int st = c % kLmStages;
-        if (!mbar_wait(&bars->full[st], (c / kLmStages) & 1, abort, budget)) {
-          fail();
-          break;
-        }
-        tc_fence_after();
-        const uint64_t a = sdesc_sw128(smem_u32(sA(st)), 16, 1024);
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          const uint64_t bdesc = sdesc_sw128(smem_u32(sB(st, n)), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < kLmK / 16; ++kk)   // +32 bytes along K = +2 in the descriptor
-            mma_bf16_ss(tmem + n * kLmN, a + 2 * kk, bdesc + 2 * kk, idesc, (c > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bars->empty[st]);
+    // The whole warp runs the loop; elect.sync inside each MMA / commit picks
+    // the issuing lane (the same one every time), so no divergent branch
+    // surrounds the issue.
+    constexpr uint32_t idesc = idesc_bf16(kLmRows, kLmN, 0, 0);
+    for (int c = 0; c < nk; ++c) {
+      const int st = c % kLmStages;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars->full[st], (c / kLmStages) & 1, abort, budget))) {
+        if (lane == 0) fail();
+        break;
       }
-      mma_commit(&bars->done);   // also after a failure: completes once issued MMAs retire
+      tc_fence_after();
+      const uint64_t a = sdesc_sw128(smem_u32(sA(st)), 16, 1024);
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        const uint64_t bdesc = sdesc_sw128(smem_u32(sB(st, n)), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kLmK / 16; ++kk)   // +32 bytes along K = +2 in the descriptor
+          mma_bf16_ss_warp(tmem + n * kLmN, a + 2 * kk, bdesc + 2 * kk, idesc, c > 0 || kk > 0);
+      }
+      mma_commit_warp(&bars->empty[st]);
     }
+    mma_commit_warp(&bars->done);   // also after a failure: completes once issued MMAs retire
     __syncwarp();
   } else {
     // ---- epilogue: thread tid owns row r0 + tid (TMEM lane tid) ----
