@@ -55,9 +55,6 @@ UNIT = "nodes/s"
 DEFAULT_WORKLOAD = "moe-paged"
 L2_BYTES = 129e6
 CALLS = ["jt_topw", "jt_tree_expand", "jt_tree_mask", "jt_tree_attn", "jt_tree_accept"]
-# Kernels each call launches (the acceptance call runs an argmax pass and a walk).
-KERNELS_PER_CALL = {"jt_topw": 1, "jt_tree_expand": 1, "jt_tree_mask": 1, "jt_tree_attn": 1,
-                    "jt_tree_accept": 2}
 # Sources whose change invalidates a committed DRAM-traffic figure.
 CALL_SOURCES = {
     "jt_topw": ["jt_topw.cu", "jt_rowscan.cuh"],
