@@ -7,11 +7,11 @@
 // startedourmission.github.io, "How it works", s(π(v)) equation), attach up
 // to W children, push them back, until B nodes exist or nothing is left.
 //
-// GPU design: one warp owns one sequence. Widths >= 2 pop in rounds
-// (tree_expand_rounds_kernel below: every node the heap would pop before
-// any child created in the round pops at once); the one-pop-at-a-time form
-// described here serves width 1, where the tree is a chain. Each step of a
-// pop is warp-parallel instead of a heap. The frontier (created, unpopped nodes with depth < N) lives in
+// GPU design: one warp owns one sequence. Expansions of more than 16 pops
+// go in rounds (tree_expand_rounds_kernel below: every node the heap would
+// pop before any child created in the round pops at once); the one-pop-at-
+// a-time form described here serves the others and width 1, where the tree
+// is a chain. Each step of a pop is warp-parallel instead of a heap. The frontier (created, unpopped nodes with depth < N) lives in
 // registers: node v occupies lane v & 31, slot v >> 5 (B <= 256 -> 8 slots).
 // A pop is two warp reductions: __reduce_max_sync over an order-preserving
 // uint32 key of the score, then __reduce_min_sync over the ids holding that
@@ -366,7 +366,11 @@ cudaError_t launch_tree_expand(const Ctx& c, const int32_t* tok, const float* lo
                                int32_t* depth, float* score, int32_t* n_nodes) {
   if (batch == 0) return cudaSuccess;
   const int slots = (B + 31) / 32;
-  if (W >= 2) {
+  // Rounds cost ~0.5 us each against ~0.15-0.25 us per pop: with at most 16
+  // pops (tiny and mid-batch shapes: 2.2 vs 2.8 us, 3.9 vs 4.7 us) popping one
+  // node at a time is faster; beyond that the rounds win (32 pops: 7.9 vs
+  // 7.6 us, 64 pops: 16.9 vs 6.3 us).
+  if (W >= 2 && (B + W - 1) / W > 16) {
     const size_t per_warp = rounds_words(n_depth, W, B) * sizeof(int32_t);   // <= 40 KiB
     const int warps = per_warp * kWarpsPerBlock <= 44 * 1024 ? kWarpsPerBlock : 1;
     const size_t smem = per_warp * warps;
