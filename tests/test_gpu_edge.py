@@ -103,7 +103,11 @@ def _increments(kind, rng, shape):
 @pytest.mark.parametrize("kind", ["unsorted", "near-zero", "equal", "positive", "neg-inf",
                                   "dominant"])
 @pytest.mark.parametrize("batch,N,W,B", [(3, 16, 4, 256), (5, 8, 4, 64), (2, 64, 2, 255),
-                                         (4, 6, 32, 200), (7, 3, 3, 33)])
+                                         (4, 6, 32, 200), (7, 3, 3, 33),
+                                         # more than 16 pops (rounds): depth 1 and 2 only,
+                                         # width 8 over 64 depths, width 15 (one warp a block)
+                                         (2, 1, 4, 100), (3, 2, 2, 200), (2, 64, 8, 256),
+                                         (2, 40, 15, 256)])
 def test_expand_increment_shapes(kind, batch, N, W, B):
     """Expansion is the heap's best-first order whatever the increments look like."""
     rng = np.random.default_rng(B * 31 + N * 7 + W + len(kind))

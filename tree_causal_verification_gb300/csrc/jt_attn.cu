@@ -34,14 +34,18 @@
 //              after both P V MMAs, so K tile j+2 streams in while tile j+1
 //              is still being processed;
 //   warp 11    idle (completes the third warpgroup);
-//   warp 9     TMEM owner and MMA issuer (one thread), per K/V tile j:
+//   warp 9     TMEM owner and MMA issuer, per K/V tile j:
 //              PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), where
 //              S_X = Q_X K^T (M=128, N=128, K=D, operands in shared memory)
 //              O_X += P_X V  (M=128, N=D, K=128 keys; P from TMEM, V from
 //                             shared memory, MN-major)
 //              so one tile's softmax overlaps the other tile's MMAs. Tensor
 //              ops retire in issue order, so the commit after S_X(j+1) also
-//              certifies that PV_X(j) has finished with P_X / O_X.
+//              certifies that PV_X(j) has finished with P_X / O_X. The whole
+//              warp runs the loop and elect.sync inside each MMA / commit
+//              picks the issuing lane: issued from a lane-0 branch instead,
+//              the MMAs fell behind the tensor pipe once the softmax warps
+//              shared the warp's scheduler;
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D),
 // O_B [256+D', ...) with D' = 128 for D = 128 (384..511).
 // Key-split instance (KSPLIT, chosen when the budget fits one M tile): tile
