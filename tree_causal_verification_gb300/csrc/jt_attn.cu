@@ -315,59 +315,84 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
 
 // Balanced schedule, before the attention grid: list the work items (unit,
 // chunk) of every unit, chunk count min(S, ceil(t / chunk_tiles)) for a unit
-// of t key tiles, sorted by chunk length, longest first (bitonic sort of
-// (length, item) keys in shared memory; unsorted beyond kPlanMaxSort slots),
-// into perm[0 .. units*S), -1 past the last item; and zero the per-unit
-// partial counts (a unit whose chunk 0 never runs is then left alone by the
-// merge). The counts only order the work: the attention kernel recomputes
+// of t key tiles, ordered by chunk length, longest first, into
+// perm[0 .. units*S), -1 past the last item; and zero the per-unit partial
+// counts (a unit whose chunk 0 never runs is then left alone by the merge).
+// The order is a counting sort on the length (one shared-memory atomic per
+// item for its place within its length, a block-wide scan of the counts, a
+// scatter): items of equal length may come in any order, which changes only
+// the schedule, never a result. Beyond kPlanMaxSort slots the items stay
+// unsorted. The counts only order the work: the attention kernel recomputes
 // and validates everything itself (it can only find fewer chunks, never
 // more, so every chunk it runs has an item).
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanMaxSort = 8192;
+constexpr int kPlanBuckets = 2 * kPlanThreads;   // lengths >= kPlanBuckets - 1 share the first
 
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParams p) {
-  extern __shared__ unsigned long long keys[];
+  extern __shared__ int plan_s[];   // [kPlanBuckets] counts, then [slots] (bucket << 16 | place)
+  __shared__ int warp_tot[kPlanThreads / 32];
   grid_dependency_sync();
   const int units = p.units, S = p.S, slots = units * S, tid = threadIdx.x;
-  const bool sort = slots <= kPlanMaxSort;
-  int n2 = 1;
-  while (n2 < slots) n2 <<= 1;
-  if (sort) {
-    for (int i = tid; i < n2; i += kPlanThreads) {
-      unsigned long long key = ~0ull;
-      if (i < slots) {
-        const int u = i / S, c = i % S;
-        const int mp = u % p.n_mpairs, b = (u / p.n_mpairs) / p.hkv;
-        const int n = p.n_nodes[b], L = p.prefix_len[b];
-        int t = 0;
-        if (n >= 0 && n <= p.B && L >= 0 && L <= p.Lbound) {
-          const int v0 = mp * 2 * p.npt;
-          if (v0 < n) t = (L + kTile - 1) / kTile + (min(v0 + 2 * p.npt, n) - 1 + kTile) / kTile;
-        }
-        const int k = min(S, max(1, (t + p.chunk_tiles - 1) / p.chunk_tiles));
-        if (c < k) {
-          const int len = min((t + k - 1) / k, 0xFFFF);
-          key = ((unsigned long long)(0xFFFFu - (unsigned)len) << 32) | (unsigned)i;
-        }
+  const int lane = tid & 31, warp = tid >> 5;
+  if (slots > kPlanMaxSort) {
+    for (int i = tid; i < slots; i += kPlanThreads) p.perm[i] = i;
+  } else {
+    int* cnt = plan_s;
+    int* rec = plan_s + kPlanBuckets;
+    for (int i = tid; i < kPlanBuckets; i += kPlanThreads) cnt[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < slots; i += kPlanThreads) {
+      int r = -1;
+      const int u = i / S, c = i % S;
+      const int mp = u % p.n_mpairs, b = (u / p.n_mpairs) / p.hkv;
+      const int n = p.n_nodes[b], L = p.prefix_len[b];
+      int t = 0;
+      if (n >= 0 && n <= p.B && L >= 0 && L <= p.Lbound) {
+        const int v0 = mp * 2 * p.npt;
+        if (v0 < n) t = (L + kTile - 1) / kTile + (min(v0 + 2 * p.npt, n) - 1 + kTile) / kTile;
       }
-      keys[i] = key;
+      const int k = min(S, max(1, (t + p.chunk_tiles - 1) / p.chunk_tiles));
+      if (c < k) {
+        const int len = (t + k - 1) / k;
+        const int d = kPlanBuckets - 1 - min(len, kPlanBuckets - 1);   // longest first
+        r = (d << 16) | atomicAdd(&cnt[d], 1);
+      }
+      rec[i] = r;
     }
     __syncthreads();
-    for (int k = 2; k <= n2; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = tid; i < n2; i += kPlanThreads) {
-          const int ixj = i ^ j;
-          if (ixj > i) {
-            const unsigned long long a = keys[i], c = keys[ixj];
-            if ((a > c) == ((i & k) == 0)) { keys[i] = c; keys[ixj] = a; }
-          }
-        }
-        __syncthreads();
-      }
+    // Exclusive scan of the counts: buckets 2 tid and 2 tid + 1 per thread.
+    const int c0 = cnt[2 * tid], c1 = cnt[2 * tid + 1];
+    int x = c0 + c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
     }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_tot[lane] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = x - (c0 + c1) + (warp > 0 ? warp_tot[warp - 1] : 0);
+    const int items = warp_tot[kPlanThreads / 32 - 1];
+    __syncthreads();   // every count read before the offsets overwrite them
+    cnt[2 * tid] = excl;
+    cnt[2 * tid + 1] = excl + c0;
+    __syncthreads();
+    for (int i = tid; i < slots; i += kPlanThreads) {
+      const int r = rec[i];
+      if (r >= 0) p.perm[cnt[r >> 16] + (r & 0xFFFF)] = i;
+    }
+    for (int i = items + tid; i < slots; i += kPlanThreads) p.perm[i] = -1;
   }
-  for (int i = tid; i < slots; i += kPlanThreads)
-    p.perm[i] = !sort ? i : keys[i] == ~0ull ? -1 : (int)(keys[i] & 0xFFFFFFFFull);
   if (p.nparts)
     for (int i = tid; i < units; i += kPlanThreads) p.nparts[i] = 0;
 }
@@ -1104,9 +1129,8 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
     p.perm = static_cast<int32_t*>(c.workspace);
     p.nparts = sc.S > 1 ? p.perm + (size_t)units * sc.S : nullptr;
     p.part = sc.S > 1 ? reinterpret_cast<float*>(static_cast<char*>(c.workspace) + meta) : nullptr;
-    int n2 = 1;
-    while (n2 < units * sc.S) n2 <<= 1;
-    const size_t plan_smem = units * sc.S <= kPlanMaxSort ? (size_t)n2 * 8 : 0;
+    const size_t plan_smem =
+        units * sc.S <= kPlanMaxSort ? (size_t)(kPlanBuckets + units * sc.S) * sizeof(int) : 0;
     if (plan_smem > 48 * 1024) {
       e = cudaFuncSetAttribute(attn_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)plan_smem);
