@@ -163,6 +163,7 @@ accept_walk_kernel(const void* __restrict__ am, int nparts, const int32_t* __res
 }
 
 constexpr int kPathThreads = 256;
+constexpr int kPathUnroll = 8;   // float4 loads in flight per thread (4: MoE-shaped 31.3 us, 8: 27.8, 16: 30.9)
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -224,20 +225,20 @@ accept_path_kernel(const float* __restrict__ target, const int32_t* __restrict__
     const GumbelKeys gk{seed, ((uint64_t)b * (B + 1) + row) << 32, inv_t};
     float bv = -INFINITY;
     int bi = INT_MAX;
-    for (int j0 = lo + tid; j0 < hi; j0 += 4 * kPathThreads) {
-      float4 x[4];
+    for (int j0 = lo + tid; j0 < hi; j0 += kPathUnroll * kPathThreads) {
+      float4 x[kPathUnroll];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kPathUnroll; ++u) {
         const int j = j0 + u * kPathThreads;
         x[u] = j < hi ? ld_stream(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
       if (SAMPLED) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < kPathUnroll; ++u)
           if (j0 + u * kPathThreads < hi) x[u] = gk(x[u], j0 + u * kPathThreads);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kPathUnroll; ++u) {
         const int j = j0 + u * kPathThreads;
         if (j < hi) {
           if (x[u].x > bv || bi == INT_MAX) { bv = x[u].x; bi = 4 * j; }
