@@ -76,6 +76,8 @@ using namespace sm100;
 
 constexpr int kThreads = 384;
 constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104, kRegsLaunch = 168;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * kRegsLaunch,
+              "the setmaxnreg split must use exactly the launch allocation");
 constexpr int kWarpTMA = 8, kWarpMMA = 9, kWarpTMAV = 10;
 constexpr int kTile = 128;                 // query rows per M tile = keys per K/V tile
 constexpr int kStages = 2;
@@ -1107,6 +1109,23 @@ size_t balanced_meta_bytes(int units, int S) {
 template <int D>
 size_t smem_bytes() { return (2 + 2 * kStages) * (size_t)kTile * D * 2 + 256 + 1024; }
 
+// Registers per thread a kernel launches with (queried once per kernel).
+cudaError_t kernel_regs(const void* kern, int* regs) {
+  static std::mutex mu;
+  static const void* keys[16] = {};
+  static int vals[16] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < 16 && keys[i]; ++i)
+    if (keys[i] == kern) { *regs = vals[i]; return cudaSuccess; }
+  cudaFuncAttributes fa = {};
+  const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  *regs = fa.numRegs;
+  for (int i = 0; i < 16; ++i)
+    if (!keys[i]) { keys[i] = kern; vals[i] = fa.numRegs; break; }
+  return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
   const size_t smem = smem_bytes<D>();
@@ -1176,6 +1195,16 @@ cudaError_t launch_d(const Ctx& c, const jt_attn_args& a, AttnParams& p) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+
+  // setmaxnreg.inc waits without bound for the registers it asks for, and
+  // the split draws on the block's launch allocation: a build whose kernel
+  // got fewer than kRegsLaunch registers per thread would never finish.
+  // Refuse it instead.
+  int regs = 0;
+  e = kernel_regs(reinterpret_cast<const void*>(kern), &regs);
+  if (e != cudaSuccess) return e;
+  if (regs * kThreads < 256 * (int)kRegsSoftmax + 128 * (int)kRegsOther)
+    return cudaErrorInvalidConfiguration;
 
   CUtensorMap mq, mkc, mvc, mkt, mvt;
   const uint64_t D64 = D;
