@@ -225,7 +225,7 @@ constexpr int kMergeRows = 2 * kTile / kMergeSlices;
 template <int D, int UN, int KMAX>
 __device__ __forceinline__ void merge_rows(const AttnParams& p, const float* part0, int k,
                                            int r0, int r1, int v0, int b, int kh,
-                                           const float* fac) {
+                                           const float* fac, uint2* tile) {
   constexpr int PF4 = part_floats<D>() / 4;
   const int g = p.g, rows = r1 - r0, items = rows * (D / 4);
   const float4* src0 = reinterpret_cast<const float4*>(part0);
@@ -255,17 +255,25 @@ __device__ __forceinline__ void merge_rows(const AttnParams& p, const float* par
             acc.z += f * x[u][s2].z; acc.w += f * x[u][s2].w;
           }
         }
-        const int vv = v0 + r / g, jh = r % g;
-        reinterpret_cast<uint2*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[c4] =
-            make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+        tile[(r - r0) * (D / 4) + c4] = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
       }
     }
+  }
+  // The partials are read row-contiguous; the output rows are written whole
+  // (16-byte stores, consecutive threads along a row) from the staged tile.
+  __syncthreads();
+  for (int i = threadIdx.x; i < rows * (D / 8); i += kMergeThreads) {
+    const int rr = i / (D / 8), q = i % (D / 8), r = r0 + rr;
+    const int vv = v0 + r / g, jh = r % g;
+    reinterpret_cast<uint4*>(p.out + (((size_t)b * p.B + vv) * p.hq + kh * g + jh) * D)[q] =
+        reinterpret_cast<const uint4*>(tile + rr * (D / 4))[q];
   }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p) {
   __shared__ float fac[kMergeRows * 8];
+  __shared__ uint2 tile[kMergeRows * (D / 4)];   // the slice's output rows, bf16
   constexpr int PF = part_floats<D>();
   grid_dependency_sync();
   const int unit = blockIdx.x / kMergeSlices, slice = blockIdx.x % kMergeSlices;
@@ -300,9 +308,9 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
   }
   __syncthreads();
   if (r1 > r0) {
-    if (k <= 2) merge_rows<D, 4, 2>(p, part0, k, r0, r1, v0, b, kh, fac);
-    else if (k <= 4) merge_rows<D, 2, 4>(p, part0, k, r0, r1, v0, b, kh, fac);
-    else merge_rows<D, 1, 8>(p, part0, k, r0, r1, v0, b, kh, fac);
+    if (k <= 2) merge_rows<D, 4, 2>(p, part0, k, r0, r1, v0, b, kh, fac, tile);
+    else if (k <= 4) merge_rows<D, 2, 4>(p, part0, k, r0, r1, v0, b, kh, fac, tile);
+    else merge_rows<D, 1, 8>(p, part0, k, r0, r1, v0, b, kh, fac, tile);
   }
   // This slice's rows of unused budget slots (node < B): zeros.
   const int z0 = max(r0, n_live), z1 = r0 + kMergeRows;
