@@ -41,6 +41,33 @@ def test_topw_random(batch, N, V, W, sigma):
     assert np.abs(to_np(logp) - logp_o).max() <= LOGP_ABS
 
 
+@pytest.mark.parametrize("rows,V,W,ent", [
+    (4, 60004, 4, False), (4, 60004, 4, True), (3, 151936, 32, True), (1, 28672, 1, False),
+    (2, 100000, 8, True), (5, 49156, 16, False), (640, 16384, 16, True), (600, 12292, 2, False)])
+def test_topw_streaming_shapes(rows, V, W, ent):
+    """Segments longer than the register-resident scan holds.
+
+    Few rows take the shared-memory ring, many rows the register double
+    buffer; the segment lengths leave ragged last batches (down to one
+    float4 in one lane). Row 0 starts with a run of -inf, row 1 holds
+    integer values (ties everywhere).
+    """
+    rng = np.random.default_rng(rows * 7 + V + W)
+    x = (rng.standard_normal((rows, 1, V)) * 3.0).astype(np.float32)
+    x[0, 0, : V // 5] = -np.inf
+    if rows > 1:
+        x[1, 0] = rng.integers(-4, 4, V).astype(np.float32)
+    tok_o, logp_o = oracle.topw(x, W)
+    xd = torch.from_numpy(x).to(DEV)
+    if ent:
+        tok, logp, h = jtree.jt_topw(xd, W, with_entropy=True)
+        assert np.abs(to_np(h) - oracle.row_entropy(x)).max() <= 2e-4
+    else:
+        tok, logp = jtree.jt_topw(xd, W)
+    assert np.array_equal(to_np(tok), tok_o)
+    assert np.abs(to_np(logp) - logp_o).max() <= LOGP_ABS
+
+
 def test_topw_ties_and_neg_inf():
     V = 4096
     x = np.zeros((4, 1, V), np.float32)

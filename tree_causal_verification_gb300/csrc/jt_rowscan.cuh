@@ -3,11 +3,14 @@
 //
 // Work layout: a row of V floats is cut into S segments (S = the cluster
 // size, 1..16); each CTA of a thread-block cluster streams one segment with
-// 128-bit non-allocating loads, two batches of float4s per thread in flight.
-// Per thread: a sorted top-K list in registers, guarded by a one-compare
-// rejection test of each float4's maximum against the current K-th value,
-// and an online log-sum-exp in the log2 domain (optionally with the sum that
-// gives the distribution's entropy).
+// 128-bit non-allocating loads: short segments all at once into registers,
+// long ones two batches of float4s per thread in flight (in registers, or
+// more through a per-thread shared-memory ring filled by cp.async).
+// Long segments keep one sorted top-K list per warp (entry k in lane k): a
+// batch costs one vote unless some float4's maximum can beat the list's K-th
+// entry, and an insertion is a warp-uniform ballot and one-lane shift.
+// Every thread keeps an online log-sum-exp in the log2 domain (optionally
+// with the sum that gives the distribution's entropy).
 //
 // Selection (warp, then block, then cluster) runs K rounds of a warp-wide
 // argmax: every lane offers its best remaining candidate; __reduce_max_sync
@@ -43,17 +46,12 @@ struct TopK {
   int i[K];
   int n;      // real elements inserted so far (the first K always enter)
   float thr;  // v[K-1] once K elements are in, NaN before (every test passes)
-  // Warp-wide pruning bound: the K-th best value of the warp so far (over
-  // the union of the lanes' lists). An element strictly below it ranks after
-  // K elements the warp already holds, so it cannot be in the warp's top K.
-  float wthr;
 
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int k = 0; k < K; ++k) { v[k] = -INFINITY; i[k] = INT_MAX; }
     n = 0;
     thr = __int_as_float(0x7fffffff);
-    wthr = -INFINITY;
   }
 
   // Elements must arrive in increasing index order within a thread, so a
@@ -187,73 +185,189 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float(u);
 }
 
-// One batch of kScanBatch float4s (element index 4*j of float4 j = j0 + u*T).
-// refresh: every lane of the warp processes a batch in this call and the
-// warp-wide pruning bound is recomputed afterwards (K rounds of warp argmax,
-// so it is done only while the bound is still tightening quickly).
-template <int K, bool LSE, bool ENT>
-__device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0, TopK<K>& top,
-                                           Lse& lse, bool refresh) {
-  float mx[kScanBatch];
+// The warp's best K elements so far for the streaming scans, one list per
+// warp: entry k (k-th by rank) in lane k, lanes >= K unused; (tv, ti) is
+// entry K-1 in every lane, the sentinel (-inf, INT_MAX) until K elements
+// have entered. A float4 is offered to the list only when it can hold an
+// element ranking before entry K-1, so after the first batches almost every
+// batch costs one vote; an insertion is warp-uniform (a ballot and a shift
+// by one lane), never a divergent per-lane sort.
+template <int K>
+struct WarpTopK {
+  static_assert(K >= 1 && K <= 32, "one entry per lane");
+  float v, tv;
+  int i, ti;
+
+  __device__ __forceinline__ void init() {
+    v = -INFINITY; i = INT_MAX;
+    tv = -INFINITY; ti = INT_MAX;
+  }
+
+  // Inserts (x, e); every lane passes the same pair.
+  __device__ __forceinline__ void insert(float x, int e) {
+    constexpr unsigned kFull = 0xFFFFFFFFu;
+    const int lane = threadIdx.x & 31;
+    // The entries are sorted, so the ones (x, e) ranks before are a suffix.
+    const uint32_t bm = __ballot_sync(kFull, lane < K && ranks_before(x, e, v, i));
+    if (bm == 0) return;
+    const int pos = __ffs(bm) - 1;
+    const float pv = __shfl_up_sync(kFull, v, 1);
+    const int pi = __shfl_up_sync(kFull, i, 1);
+    if (lane == pos) {
+      v = x; i = e;
+    } else if (lane > pos && lane < K) {
+      v = pv; i = pi;
+    }
+    tv = __shfl_sync(kFull, v, K - 1);
+    ti = __shfl_sync(kFull, i, K - 1);
+  }
+
+  // The K-th largest of the warp's valid float4 maxima (-inf if there are
+  // fewer than K): K float4s each hold an element at least that large, so
+  // no element below it can end in the warp's top K.
+  __device__ __forceinline__ static float kth_max(const float (&mx)[kScanBatch], uint32_t valid) {
+    constexpr unsigned kFull = 0xFFFFFFFFu;
+    static_assert(kScanBatch == 4, "sorting network for four values");
+    float s0 = (valid & 1u) ? mx[0] : -INFINITY, s1 = (valid & 2u) ? mx[1] : -INFINITY;
+    float s2 = (valid & 4u) ? mx[2] : -INFINITY, s3 = (valid & 8u) ? mx[3] : -INFINITY;
+    float t;
+    t = fmaxf(s0, s1); s1 = fminf(s0, s1); s0 = t;
+    t = fmaxf(s2, s3); s3 = fminf(s2, s3); s2 = t;
+    t = fmaxf(s0, s2); s2 = fminf(s0, s2); s0 = t;
+    t = fmaxf(s1, s3); s3 = fminf(s1, s3); s1 = t;
+    t = fmaxf(s1, s2); s2 = fminf(s1, s2); s1 = t;
+    const int n = __popc(valid);
+    int h = 0;
+    uint32_t top = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const float hv = h == 0 ? s0 : h == 1 ? s1 : h == 2 ? s2 : s3;
+      const uint32_t key = h < n ? order_key(hv) : 0u;
+      top = __reduce_max_sync(kFull, key);
+      if (top == 0u) return -INFINITY;
+      const uint32_t win = __ballot_sync(kFull, key == top);
+      if ((threadIdx.x & 31) == __ffs(win) - 1) ++h;
+    }
+    return key_value(top);
+  }
+
+  // Offers the valid float4s of one batch (float4 u of this lane has index
+  // j0 + u*T, its maximum mx[u]).
+  __device__ __forceinline__ void offer(const float4 (&x)[kScanBatch], const float (&mx)[kScanBatch],
+                                        uint32_t valid, int j0) {
+    constexpr unsigned kFull = 0xFFFFFFFFu;
+    const int lane = threadIdx.x & 31;
+    const float bound = ti == INT_MAX ? kth_max(mx, valid) : tv;
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u)
+      m |= (uint32_t)(((valid >> u) & 1u) && mx[u] >= bound) << u;
+    if (!__any_sync(kFull, m != 0)) return;
+    // Exact test against entry K-1: a larger maximum, or an equal one whose
+    // first index is lower.
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u)
+      if (!(mx[u] > tv || 4 * (j0 + u * kScanThreads) < ti)) m &= ~(1u << u);
+    for (;;) {
+      const uint32_t lanes = __ballot_sync(kFull, m != 0);
+      if (lanes == 0) break;
+      const int src = __ffs(lanes) - 1;
+      const int u = __shfl_sync(kFull, __ffs(m) - 1, src);
+      float4 q = x[0];
+#pragma unroll
+      for (int w = 1; w < kScanBatch; ++w)
+        if (w == u) q = x[w];
+      q.x = __shfl_sync(kFull, q.x, src);
+      q.y = __shfl_sync(kFull, q.y, src);
+      q.z = __shfl_sync(kFull, q.z, src);
+      q.w = __shfl_sync(kFull, q.w, src);
+      const int e = 4 * (__shfl_sync(kFull, j0, src) + u * kScanThreads);
+      insert(q.x, e);
+      insert(q.y, e + 1);
+      insert(q.z, e + 2);
+      insert(q.w, e + 3);
+      if (lane == src) m &= m - 1;
+    }
+  }
+};
+
+// Adds the valid float4s of a batch (bits of `valid`; all of them when
+// valid == 0xF) to the thread's log-sum-exp.
+template <bool ENT>
+__device__ __forceinline__ void lse_batch(const float4 (&x)[kScanBatch], const float (&mx)[kScanBatch],
+                                          uint32_t valid, Lse& lse) {
+  float bm = -INFINITY;
 #pragma unroll
   for (int u = 0; u < kScanBatch; ++u)
-    mx[u] = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
-  if (LSE) {
-    const float bm2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * kLog2e;
-    if (bm2 > lse.m) lse.raise<ENT>(bm2);
-    if (lse.m != -INFINITY) {
-      const float nm = -lse.m;
-      float a0 = 0.0f, a1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
+    if ((valid >> u) & 1u) bm = fmaxf(bm, mx[u]);
+  const float bm2 = bm * kLog2e;
+  if (bm2 > lse.m) lse.raise<ENT>(bm2);
+  if (lse.m != -INFINITY) {
+    const float nm = -lse.m;
+    float a0 = 0.0f, a1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
 #pragma unroll
-      for (int u = 0; u < kScanBatch; ++u) {
+    for (int u = 0; u < kScanBatch; ++u) {
+      if ((valid >> u) & 1u) {
         a0 += lse.term<ENT>(fmaf(x[u].x, kLog2e, nm), t0) +
               lse.term<ENT>(fmaf(x[u].y, kLog2e, nm), t1);
         a1 += lse.term<ENT>(fmaf(x[u].z, kLog2e, nm), t0) +
               lse.term<ENT>(fmaf(x[u].w, kLog2e, nm), t1);
       }
-      lse.s += a0 + a1;
-      if (ENT) lse.t += t0 + t1;
     }
-  }
-#pragma unroll
-  for (int u = 0; u < kScanBatch; ++u) {
-    // Some element of this float4 may enter: above the lane's own K-th value
-    // and not below the warp's bound.
-    if (mx[u] >= top.wthr && !(mx[u] <= top.thr)) {
-      const int e = 4 * (j0 + u * kScanThreads);
-      top.push(x[u].x, e);
-      top.push(x[u].y, e + 1);
-      top.push(x[u].z, e + 2);
-      top.push(x[u].w, e + 3);
-    }
-  }
-  if (refresh) {
-    float wv[K];
-    int wi[K];
-    warp_select<K, K>(top.v, top.i, min(top.n, K), wv, wi);
-    top.wthr = wv[K - 1];   // -inf while the warp holds fewer than K elements
+    lse.s += a0 + a1;
+    if (ENT) lse.t += t0 + t1;
   }
 }
 
-// Streams float4s [lo4, hi4) of `row` into per-thread state: full batches
-// without bounds checks, ping-ponging two register buffers so that one batch
-// is in flight while the other is processed, then a checked tail.
+// One full batch of kScanBatch float4s (float4 j0 + u*T for u < kScanBatch);
+// warp-collective.
+template <int K, bool LSE, bool ENT>
+__device__ __forceinline__ void scan_batch(const float4 (&x)[kScanBatch], int j0, WarpTopK<K>& top,
+                                           Lse& lse) {
+  float mx[kScanBatch];
+#pragma unroll
+  for (int u = 0; u < kScanBatch; ++u)
+    mx[u] = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+  if (LSE) lse_batch<ENT>(x, mx, 0xFu, lse);
+  top.offer(x, mx, 0xFu, j0);
+}
+
+// The last, partial batch of a segment: float4s full_end + tid + u*T below
+// hi4 hold data, the rest is padding that neither enters the list nor the
+// sums. Warp-collective: every lane calls it, lanes with padding only too.
+template <int K, bool LSE, bool ENT>
+__device__ __forceinline__ void scan_tail(const float4 (&x)[kScanBatch], int full_end, int hi4,
+                                          WarpTopK<K>& top, Lse& lse) {
+  const int tid = (int)threadIdx.x;
+  uint32_t valid = 0;
+  float mx[kScanBatch];
+#pragma unroll
+  for (int u = 0; u < kScanBatch; ++u) {
+    const bool ok = full_end + tid + u * kScanThreads < hi4;
+    valid |= (uint32_t)ok << u;
+    mx[u] = ok ? fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)) : -INFINITY;
+  }
+  if (LSE) lse_batch<ENT>(x, mx, valid, lse);
+  top.offer(x, mx, valid, full_end + tid);
+}
+
+// Streams float4s [lo4, hi4) of `row` into the warp lists and the threads'
+// sums: full batches without bounds checks, ping-ponging two register
+// buffers so that one batch is in flight while the other is processed, then
+// a checked tail. Every lane of a warp runs the same batches (the warp-wide
+// list needs the whole warp).
 // EARLY_TAIL: a segment of at most two full batches issues its tail's loads
 // together with them (one round trip to memory instead of two); measured to
 // pay off for the plain argmax only, the log-sum-exp and keyed scans lose.
 template <int K, bool LSE, bool ENT = false, class Xf = IdentityXf, bool EARLY_TAIL = false>
 __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int lo4, int hi4,
-                                             TopK<K>& top, Lse& lse, const Xf& xf = Xf()) {
+                                             WarpTopK<K>& top, Lse& lse, const Xf& xf = Xf()) {
   const float4* r4 = reinterpret_cast<const float4*>(row);
   constexpr int STEP = kScanThreads * kScanBatch;
   const int tid = (int)threadIdx.x;
   const int full_end = lo4 + ((hi4 - lo4) / STEP) * STEP;
   float4 a[kScanBatch], b[kScanBatch];
   int base = lo4;
-  // Full batches are uniform over the CTA; the warp bound is refreshed after
-  // batches 1, 2, 4, 8, ... (a stale bound is still a valid, looser bound).
-  int nbatch = 0;
-  auto refresh = [&]() { ++nbatch; return (nbatch & (nbatch - 1)) == 0; };
   if (base < full_end) {
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u) a[u] = ld_stream(r4 + base + tid + u * kScanThreads);
@@ -279,7 +393,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
     }
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u) a[u] = xf(a[u], base + tid + u * kScanThreads);
-    scan_batch<K, LSE, ENT>(a, base + tid, top, lse, refresh());
+    scan_batch<K, LSE, ENT>(a, base + tid, top, lse);
     base += STEP;
     if (!nb) break;
     const bool na = base + STEP < full_end;
@@ -289,7 +403,7 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
     }
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u) b[u] = xf(b[u], base + tid + u * kScanThreads);
-    scan_batch<K, LSE, ENT>(b, base + tid, top, lse, refresh());
+    scan_batch<K, LSE, ENT>(b, base + tid, top, lse);
     base += STEP;
     if (!na) break;
   }
@@ -302,54 +416,90 @@ __device__ __forceinline__ void scan_segment(const float* __restrict__ row, int 
       const int j = full_end + tid + u * kScanThreads;
       a[u] = j < hi4 ? xf(early_tail ? tl[u] : ld_stream(r4 + j), j) : ninf;
     }
-    if (full_end + tid < hi4) {
-      // Lanes whose whole batch is padding skip it (their padding would
-      // otherwise occupy top-K slots as if they were real -inf elements).
-      float4 x[kScanBatch];
-      int cnt = 0;
+    scan_tail<K, LSE, ENT>(a, full_end, hi4, top, lse);
+  }
+}
+
+// 16-byte asynchronous copy global -> shared that bypasses L1 (cp.async.cg);
+// its completion is tracked per thread by commit groups.
+__device__ __forceinline__ void cp_async16(float4* dst, const float4* src) {
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's commit groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Dynamic shared memory of the ring scan: NST stages of one batch.
+template <int NST>
+constexpr size_t ring_smem_bytes() {
+  return (size_t)NST * kScanBatch * kScanThreads * sizeof(float4);
+}
+
+// scan_segment with the batches staged in shared memory instead of
+// registers: every thread copies its own float4s of batch c into stage
+// c mod NST with cp.async and reads them back once the copy has landed, so
+// NST batches (NST x 16 KB per CTA) are in flight without holding registers.
+// No thread reads another's data, so the only synchronisation is the
+// thread's own cp.async.wait_group. The tail (the last, partial batch) goes
+// through the ring as well. `ring` holds NST * kScanBatch * kScanThreads
+// float4s.
+template <int K, bool LSE, bool ENT, int NST>
+__device__ __forceinline__ void scan_segment_ring(const float* __restrict__ row, int lo4, int hi4,
+                                                  WarpTopK<K>& top, Lse& lse, float4* ring) {
+  static_assert(NST >= 2, "the ring needs two stages at least");
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  constexpr int STEP = kScanThreads * kScanBatch;
+  const int tid = (int)threadIdx.x;
+  const int nfull = (hi4 - lo4) / STEP;
+  const int full_end = lo4 + nfull * STEP;
+  const int nb = nfull + (full_end < hi4 ? 1 : 0);
+  float4* mine = ring + tid;
+  // Batch c -> stage c mod NST; the thread's float4 u of a stage sits at
+  // (stage * kScanBatch + u) * kScanThreads (consecutive threads, consecutive
+  // 16-byte words: no bank conflicts).
+  auto issue = [&](int c, int stage) {
+    if (c < nb) {
+      const int j0 = lo4 + c * STEP + tid;
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) {
-        const int j = full_end + tid + u * kScanThreads;
-        x[u] = a[u];
-        cnt += j < hi4;
-      }
-      if (cnt == kScanBatch) {
-        scan_batch<K, LSE, ENT>(x, full_end + tid, top, lse, false);
-      } else {
-        // Partial batch: element-wise, in index order.
-        if (LSE) {
-          float bm = -INFINITY;
-#pragma unroll
-          for (int u = 0; u < kScanBatch; ++u)
-            if (u < cnt) bm = fmaxf(bm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
-          const float bm2 = bm * kLog2e;
-          if (bm2 > lse.m) lse.raise<ENT>(bm2);
-          if (lse.m != -INFINITY) {
-            const float nm = -lse.m;
-            float acc = 0.0f, tacc = 0.0f;
-#pragma unroll
-            for (int u = 0; u < kScanBatch; ++u)
-              if (u < cnt)
-                acc += lse.term<ENT>(fmaf(x[u].x, kLog2e, nm), tacc) +
-                       lse.term<ENT>(fmaf(x[u].y, kLog2e, nm), tacc) +
-                       lse.term<ENT>(fmaf(x[u].z, kLog2e, nm), tacc) +
-                       lse.term<ENT>(fmaf(x[u].w, kLog2e, nm), tacc);
-            lse.s += acc;
-            if (ENT) lse.t += tacc;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kScanBatch; ++u) {
-          if (u < cnt) {
-            const int e = 4 * (full_end + tid + u * kScanThreads);
-            top.push(x[u].x, e);
-            top.push(x[u].y, e + 1);
-            top.push(x[u].z, e + 2);
-            top.push(x[u].w, e + 3);
-          }
-        }
+        const int j = j0 + u * kScanThreads;
+        if (c < nfull || j < hi4) cp_async16(mine + (stage * kScanBatch + u) * kScanThreads, r4 + j);
       }
     }
+    cp_async_commit();   // an empty group past the end keeps the count uniform
+  };
+#pragma unroll
+  for (int c = 0; c < NST - 1; ++c) issue(c, c);
+  int stage = 0, fill = NST - 1;
+  for (int c = 0; c < nfull; ++c) {
+    // Stage `fill` held batch c - 1, which this thread has consumed.
+    issue(c + NST - 1, fill);
+    fill = fill + 1 == NST ? 0 : fill + 1;
+    cp_async_wait<NST - 1>();   // batch c has landed
+    float4 x[kScanBatch];
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) x[u] = mine[(stage * kScanBatch + u) * kScanThreads];
+    stage = stage + 1 == NST ? 0 : stage + 1;
+    scan_batch<K, LSE, ENT>(x, lo4 + c * STEP + tid, top, lse);
+  }
+  cp_async_wait<0>();
+  if (full_end < hi4) {
+    float4 x[kScanBatch];
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) {
+      const int j = full_end + tid + u * kScanThreads;
+      x[u] = j < hi4 ? mine[(stage * kScanBatch + u) * kScanThreads]
+                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    scan_tail<K, LSE, ENT>(x, full_end, hi4, top, lse);
   }
 }
 
@@ -504,14 +654,18 @@ __device__ __forceinline__ void block_reduce_lists(const float (&wv)[K], const i
   __syncthreads();
 }
 
-// Reduces the CTA's per-thread state into `out` (valid after the trailing
-// __syncthreads).
+// Reduces the warps' lists and the threads' sums into `out` (valid after
+// the trailing __syncthreads).
 template <int K, bool LSE>
-__device__ __forceinline__ void block_reduce(TopK<K>& top, Lse& lse, ScanPartial<K>* out,
-                                             ScanPartial<K>* warp_parts) {
+__device__ __forceinline__ void block_reduce(const WarpTopK<K>& top, Lse& lse,
+                                             ScanPartial<K>* out, ScanPartial<K>* warp_parts) {
   float wv[K];
   int wi[K];
-  warp_select<K, K>(top.v, top.i, min(top.n, K), wv, wi);
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    wv[k] = __shfl_sync(0xFFFFFFFFu, top.v, k);
+    wi[k] = __shfl_sync(0xFFFFFFFFu, top.i, k);
+  }
   block_reduce_lists<K, LSE>(wv, wi, lse, out, warp_parts);
 }
 
@@ -534,11 +688,25 @@ __device__ __forceinline__ void scan_to_partial(const float* __restrict__ row, i
     scan_resident<K, LSE, ENT>(row, lo4, hi4, wv, wi, lse, xf);
     block_reduce_lists<K, LSE>(wv, wi, lse, part, warp_parts);
   } else {
-    TopK<K> top;
+    WarpTopK<K> top;
     top.init();
     scan_segment<K, LSE, ENT, Xf, EARLY_TAIL>(row, lo4, hi4, top, lse, xf);
     block_reduce<K, LSE>(top, lse, part, warp_parts);
   }
+}
+
+// The streaming scan of [lo4, hi4) through a shared-memory ring (NST
+// stages at `ring`) into `part`.
+template <int K, bool LSE, bool ENT, int NST>
+__device__ __forceinline__ void scan_to_partial_ring(const float* __restrict__ row, int lo4,
+                                                     int hi4, ScanPartial<K>* part,
+                                                     ScanPartial<K>* warp_parts, float4* ring) {
+  Lse lse;
+  lse.init();
+  WarpTopK<K> top;
+  top.init();
+  scan_segment_ring<K, LSE, ENT, NST>(row, lo4, hi4, top, lse, ring);
+  block_reduce<K, LSE>(top, lse, part, warp_parts);
 }
 
 // Merges the cluster's partials in CTA rank 0 (warp 0). Returns true in the

@@ -14,24 +14,33 @@
 // cluster when there are too few rows to fill the GPU (batch 1: 16 rows of
 // 151936 logits -> 16-CTA clusters), and the cluster merges its partials in
 // distributed shared memory.
+#include <atomic>
+
 #include "jt_rowscan.cuh"
 
 namespace jt {
 namespace {
 
-template <int K, bool ENT, bool RES>
+// NST > 0: the streaming scan stages its batches in an NST-stage shared-
+// memory ring (dynamic shared memory) instead of registers.
+template <int K, bool ENT, bool RES, int NST>
 __global__ void __launch_bounds__(kScanThreads)
 topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __restrict__ tok,
             float* __restrict__ logp, float* __restrict__ entropy) {
   __shared__ ScanPartial<K> warp_parts[kScanWarps];
   __shared__ ScanPartial<K> part;
+  extern __shared__ __align__(16) float4 ring[];
   const int row = blockIdx.x / S;
   const int seg = blockIdx.x % S;
   const int v4 = V >> 2;
   const int per = (v4 + S - 1) / S;
   const int lo = min(v4, seg * per), hi = min(v4, lo + per);
   grid_dependency_sync();
-  scan_to_partial<K, true, ENT, RES>(logits + (size_t)row * V, lo, hi, &part, warp_parts);
+  if constexpr (NST > 0)
+    scan_to_partial_ring<K, true, ENT, NST>(logits + (size_t)row * V, lo, hi, &part, warp_parts,
+                                            ring);
+  else
+    scan_to_partial<K, true, ENT, RES>(logits + (size_t)row * V, lo, hi, &part, warp_parts);
   TopK<K> top;
   Lse lse;
   if (cluster_reduce<K, true>(&part, S, top, lse)) {
@@ -51,13 +60,48 @@ topw_kernel(const float* __restrict__ logits, int V, int W, int S, int32_t* __re
   }
 }
 
+// The shared-memory ring: kRingStages batches of 16 KB per CTA, two CTAs per
+// SM. It is used for streaming scans whose rows fill at most two CTAs per SM
+// (one wave of few, long segments), where the two register batches of the
+// plain streaming scan keep too few bytes in flight per CTA; such rows are
+// then cut into as many segments as keep that bound.
+constexpr int kRingStages = 6;
+constexpr int kRingCtasPerSm = 2;
+
+template <int K, bool ENT>
+cudaError_t launch_ring(const Ctx& c, const float* logits, int rows, int V, int W, int S,
+                        int32_t* tok, float* logp, float* entropy) {
+  auto kern = topw_kernel<K, ENT, false, kRingStages>;
+  constexpr size_t smem = ring_smem_bytes<kRingStages>();
+  static std::atomic<uint64_t> opted{0};   // devices the shared-memory limit was raised on
+  const uint64_t bit = 1ull << (c.device & 63);
+  if (!(opted.load(std::memory_order_relaxed) & bit)) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    opted.fetch_or(bit, std::memory_order_relaxed);
+  }
+  return launch_kernel(kern, dim3(rows * S), dim3(kScanThreads), smem, c.stream, S, logits, V, W,
+                       S, tok, logp, entropy);
+}
+
 template <int K>
 cudaError_t launch_k(const Ctx& c, const float* logits, int rows, int V, int W, int32_t* tok,
                      float* logp, float* entropy) {
-  const int S = pick_row_split(rows, V / 4, c.num_sms, 16);
-  const bool res = use_resident(K, (V / 4 + S - 1) / S);
-  auto kern = entropy ? (res ? topw_kernel<K, true, true> : topw_kernel<K, true, false>)
-                      : (res ? topw_kernel<K, false, true> : topw_kernel<K, false, false>);
+  const int v4 = V / 4;
+  const long ring_ctas = (long)kRingCtasPerSm * c.num_sms;
+  if (K <= 16 && rows <= ring_ctas) {   // (K = 32 takes too many registers for two CTAs per SM)
+    const int S = pick_row_split(rows, v4, c.num_sms, 16);
+    int Sr = 1;
+    while (2 * Sr <= S && (long)rows * 2 * Sr <= ring_ctas) Sr *= 2;
+    if (!use_resident(K, (v4 + Sr - 1) / Sr))
+      return entropy ? launch_ring<K, true>(c, logits, rows, V, W, Sr, tok, logp, entropy)
+                     : launch_ring<K, false>(c, logits, rows, V, W, Sr, tok, logp, entropy);
+  }
+  const int S = pick_row_split(rows, v4, c.num_sms, 16);
+  const bool res = use_resident(K, (v4 + S - 1) / S);
+  auto kern = entropy ? (res ? topw_kernel<K, true, true, 0> : topw_kernel<K, true, false, 0>)
+                      : (res ? topw_kernel<K, false, true, 0> : topw_kernel<K, false, false, 0>);
   return launch_clustered(kern, rows * S, S, c.stream, logits, V, W, S, tok, logp, entropy);
 }
 
