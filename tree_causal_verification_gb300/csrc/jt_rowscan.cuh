@@ -258,16 +258,19 @@ struct WarpTopK {
     constexpr unsigned kFull = 0xFFFFFFFFu;
     const int lane = threadIdx.x & 31;
     const float bound = ti == INT_MAX ? kth_max(mx, valid) : tv;
+    float bm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u)
+      if ((valid >> u) & 1u) bm = fmaxf(bm, mx[u]);
+    // One vote per batch while no lane's batch maximum reaches the bound.
+    if (!__any_sync(kFull, (valid != 0u) && bm >= bound)) return;
+    // Float4s that can hold an element ranking before entry K-1: a larger
+    // maximum, or an equal one whose first index is lower.
     uint32_t m = 0;
 #pragma unroll
     for (int u = 0; u < kScanBatch; ++u)
-      m |= (uint32_t)(((valid >> u) & 1u) && mx[u] >= bound) << u;
-    if (!__any_sync(kFull, m != 0)) return;
-    // Exact test against entry K-1: a larger maximum, or an equal one whose
-    // first index is lower.
-#pragma unroll
-    for (int u = 0; u < kScanBatch; ++u)
-      if (!(mx[u] > tv || 4 * (j0 + u * kScanThreads) < ti)) m &= ~(1u << u);
+      m |= (uint32_t)(((valid >> u) & 1u) && mx[u] >= bound &&
+                      (mx[u] > tv || 4 * (j0 + u * kScanThreads) < ti)) << u;
     for (;;) {
       const uint32_t lanes = __ballot_sync(kFull, m != 0);
       if (lanes == 0) break;
@@ -277,15 +280,12 @@ struct WarpTopK {
 #pragma unroll
       for (int w = 1; w < kScanBatch; ++w)
         if (w == u) q = x[w];
-      q.x = __shfl_sync(kFull, q.x, src);
-      q.y = __shfl_sync(kFull, q.y, src);
-      q.z = __shfl_sync(kFull, q.z, src);
-      q.w = __shfl_sync(kFull, q.w, src);
+      const float qv[4] = {__shfl_sync(kFull, q.x, src), __shfl_sync(kFull, q.y, src),
+                           __shfl_sync(kFull, q.z, src), __shfl_sync(kFull, q.w, src)};
       const int e = 4 * (__shfl_sync(kFull, j0, src) + u * kScanThreads);
-      insert(q.x, e);
-      insert(q.y, e + 1);
-      insert(q.z, e + 2);
-      insert(q.w, e + 3);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)   // warp-uniform test: most elements of the float4 fail it
+        if (qv[c] > tv || (qv[c] == tv && e + c < ti)) insert(qv[c], e + c);
       if (lane == src) m &= m - 1;
     }
   }
