@@ -83,6 +83,7 @@ constexpr int kTile = 128;                 // query rows per M tile = keys per K
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kPrefetchPages = 3;          // block-table entries per thread loaded with the sequence sizes
 
 struct AttnParams {
   int batch, B, hq, hkv, g, npt, n_mpairs, S;
@@ -486,6 +487,16 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   const int v0 = mp * 2 * npt;
 
   // ---- validate the sequence (same verdict in every CTA of the sequence) ----
+  // The first kPrefetchPages * kThreads block-table entries of the sequence
+  // are loaded together with its node count and prefix length (they lie in
+  // the sequence's row of the table whatever the length), so that the page
+  // check costs no extra round trip; longer tables read the rest after.
+  int pre[kPrefetchPages];
+#pragma unroll
+  for (int q = 0; q < kPrefetchPages; ++q) {
+    const int i = tid + q * kThreads;
+    pre[q] = (p.paged && !no_item && i < p.max_pages) ? p.block_table[(size_t)b * p.max_pages + i] : 0;
+  }
   const int n_raw = p.n_nodes[b];
   const int L = p.prefix_len[b];
   int flag = 0;
@@ -493,7 +504,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
   if (L < 0 || L > p.Lbound) flag |= JT_DEVERR_PREFIX;
   if (p.paged && !no_item && !(flag & JT_DEVERR_PREFIX)) {
     const int np = (L + kPageSize - 1) / kPageSize;
-    for (int i = tid; i < np; i += kThreads) {
+#pragma unroll
+    for (int q = 0; q < kPrefetchPages; ++q)
+      if (tid + q * kThreads < np && (pre[q] < 0 || pre[q] >= p.n_pages)) flag |= JT_DEVERR_PAGE;
+    for (int i = tid + kPrefetchPages * kThreads; i < np; i += kThreads) {
       const int pg = p.block_table[(size_t)b * p.max_pages + i];
       if (pg < 0 || pg >= p.n_pages) flag |= JT_DEVERR_PAGE;
     }
