@@ -207,7 +207,10 @@ def test_attention_random(batch, B, n_list, hq, hkv, D, lens, paged):
 
 @pytest.mark.parametrize("batch,N,W,B,V", [(4, 4, 2, 16, 64), (3, 16, 4, 256, 1024),
                                            (5, 8, 1, 8, 4096), (2, 64, 2, 200, 512),
-                                           (17, 16, 4, 128, 2048)])
+                                           (17, 16, 4, 128, 2048),
+                                           # all-rows argmax over long, streamed segments
+                                           # (136 and 104 rows, 4 and 2 segments per row)
+                                           (3, 16, 1, 16, 151936), (2, 8, 2, 12, 100000)])
 def test_accept_random(batch, N, W, B, V):
     rng = np.random.default_rng(N * W * B)
     batch = max(batch, 8)
