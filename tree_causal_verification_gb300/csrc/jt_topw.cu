@@ -73,9 +73,11 @@ cudaError_t launch_ring(const Ctx& c, const float* logits, int rows, int V, int 
                         int32_t* tok, float* logp, float* entropy) {
   auto kern = topw_kernel<K, ENT, false, kRingStages>;
   constexpr size_t smem = ring_smem_bytes<kRingStages>();
-  static std::atomic<uint64_t> opted{0};   // devices the shared-memory limit was raised on
-  const uint64_t bit = 1ull << (c.device & 63);
-  if (!(opted.load(std::memory_order_relaxed) & bit)) {
+  // Devices 0..63 the shared-memory limit was raised on (others raise it on
+  // every launch).
+  static std::atomic<uint64_t> opted{0};
+  const uint64_t bit = (c.device >= 0 && c.device < 64) ? 1ull << c.device : 0ull;
+  if (!bit || !(opted.load(std::memory_order_relaxed) & bit)) {
     const cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
