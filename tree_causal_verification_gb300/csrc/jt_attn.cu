@@ -614,6 +614,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
       uint64_t* full = is_v ? bars->v_full : bars->k_full;
       uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
       const int np = (L + kPageSize - 1) / kPageSize;
+      // Page ids of a paged prefix tile: all eight loaded together, one tile
+      // ahead (right after the current tile's copies have taken theirs), so
+      // that they are in flight while the producer waits for the next ring
+      // slot (one at a time, each load sat between TMA issues).
+      constexpr int kPagesPerTile = kTile / kPageSize;
+      int pg_cur[kPagesPerTile];
+      auto load_pages = [&](int t, int (&ids)[kPagesPerTile]) {
+        if (p.paged && t < p_tiles) {
+#pragma unroll
+          for (int q = 0; q < kPagesPerTile; ++q) {
+            const int pi = t * kPagesPerTile + q;
+            ids[q] = pi < np ? p.block_table[(size_t)b * p.max_pages + pi] : 0;
+          }
+        }
+      };
+      load_pages(t_begin, pg_cur);
       for (int jt = 0; jt < T; ++jt) {
         const int t = t_begin + jt, st = jt % kStages;
         if (jt >= kStages &&
@@ -627,14 +643,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         if (t < p_tiles) {
           const int key0 = t * kTile;
           if (p.paged) {
-#pragma unroll 1
-            for (int pg = 0; pg < kTile / kPageSize; ++pg) {
-              const int pi = key0 / kPageSize + pg;
-              const int page = pi < np ? p.block_table[(size_t)b * p.max_pages + pi] : 0;
+#pragma unroll
+            for (int pg = 0; pg < kPagesPerTile; ++pg) {
 #pragma unroll
               for (int ch = 0; ch < CH; ++ch)
                 tma_load_4d(dst + ch * CHB + pg * (kPageSize * 128), mc, &full[st], ch * 64, kh, 0,
-                            page);
+                            pg_cur[pg]);
             }
           } else {
 #pragma unroll
@@ -647,6 +661,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
           for (int ch = 0; ch < CH; ++ch)
             tma_load_4d(dst + ch * CHB, mtr, &full[st], ch * 64, kh, u0, b);
         }
+        if (jt + 1 < T) load_pages(t + 1, pg_cur);
       }
     }
   } else if (warp == kWarpMMA) {
